@@ -1,0 +1,149 @@
+"""fp64 CPU oracle for the attention forward -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, OpenMP
+over rows); this module compiles it with gcc and marshals arguments through
+ctypes.  It shares no code with the CUDA library and imports nothing from it.
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may use it.
+
+Definition followed: "A Thread-Register Decoupled GPU Execution Model for
+Efficient Tensor Computation", Background (Equ. 1, multi-head attention) and
+Methodology (GQA / MQA head sharing, FlashDecoding for decode); the equation
+itself is not printed on the page, so the standard scaled-dot-product
+attention with a bottom-right causal mask and a natural-log LSE is written out
+in the C file's header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_vp = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_attn_fwd_rows.argtypes = [
+                _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                _dbl, _vp, _i64, _vp, _vp]
+            lib.oracle_attn_fwd_rows.restype = ctypes.c_int
+            lib.oracle_decode_split.argtypes = [
+                _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _dbl, _vp, _vp]
+            lib.oracle_decode_split.restype = ctypes.c_int
+            lib.oracle_combine.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _vp]
+            lib.oracle_combine.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """Contiguous uint16 view of a bf16 tensor (torch) or a uint16 array."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("numpy inputs must be uint16 bf16 bit patterns")
+        return np.ascontiguousarray(x)
+    import torch  # local: plain CPU tensors only
+    if x.dtype != torch.bfloat16:
+        raise TypeError("oracle inputs must be bf16")
+    return x.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_vp)
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, rows=None):
+    """O (float64 [..., D]) and LSE (float64) for Q [B,Hq,Sq,D], K/V [B,Hkv,Sk,D].
+
+    ``rows`` (optional): flat row ids (b*Hq + h)*Sq + i; then O is [n, D] and
+    LSE is [n].  Otherwise O is [B,Hq,Sq,D] and LSE is [B,Hq,Sq].
+    """
+    B, Hq, Sq, D = (int(s) for s in q.shape)
+    Bk, Hkv, Sk, Dk = (int(s) for s in k.shape)
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch")
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    if rows is None:
+        n = B * Hq * Sq
+        rp = None
+    else:
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = rows.size
+        rp = _ptr(rows)
+    o = np.empty((n, D), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    rc = _load().oracle_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sq,
+                                      Sk, D, int(bool(causal)), float(scale), rp, n,
+                                      _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_rows failed ({rc})")
+    if rows is None:
+        return o.reshape(B, Hq, Sq, D), lse.reshape(B, Hq, Sq)
+    return o, lse
+
+
+def decode_split(q, k, v, num_splits: int, scale: float):
+    """Per-split partials: O_s [ns,B,Hq,D] and LSE_s [ns,B,Hq] (float64)."""
+    B, Hq, Sq, D = (int(s) for s in q.shape)
+    if Sq != 1:
+        raise ValueError("decode takes one query row per head")
+    _, Hkv, Sk, _ = (int(s) for s in k.shape)
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    ns = int(num_splits)
+    o = np.empty((ns, B, Hq, D), dtype=np.float64)
+    lse = np.empty((ns, B, Hq), dtype=np.float64)
+    rc = _load().oracle_decode_split(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sk, D,
+                                     ns, float(scale), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_split failed ({rc})")
+    return o, lse
+
+
+def combine(o_part, lse_part):
+    """LSE combine: o_part [ns,...,D], lse_part [ns,...] -> (O [...,D], LSE [...])."""
+    o_part = np.ascontiguousarray(np.asarray(o_part, dtype=np.float64))
+    lse_part = np.ascontiguousarray(np.asarray(lse_part, dtype=np.float64))
+    ns = o_part.shape[0]
+    D = o_part.shape[-1]
+    rest = o_part.shape[1:-1]
+    R = int(np.prod(rest)) if rest else 1
+    if lse_part.shape != (ns,) + tuple(rest):
+        raise ValueError("lse_part shape mismatch")
+    o = np.empty(tuple(rest) + (D,), dtype=np.float64)
+    lse = np.empty(tuple(rest), dtype=np.float64)
+    rc = _load().oracle_combine(_ptr(o_part), _ptr(lse_part), R, D, ns, _ptr(o),
+                                _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_combine failed ({rc})")
+    return o, lse

@@ -1,0 +1,248 @@
+/*
+ * attn_oracle.c -- plain, slow, fp64 CPU oracle for the attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness reference for the
+ * CUDA library in tensor_attn_fwd_gb300/.  The two share no code, headers,
+ * helpers or constants.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load or call it; the product
+ * path never does.
+ *
+ * What it computes (source: "A Thread-Register Decoupled GPU Execution Model
+ * for Efficient Tensor Computation", Background, Equ. 1 -- the multi-head
+ * attention that the FlashAttention series computes fused; the equation is
+ * referenced there but not printed, so its standard content is written out
+ * here):
+ *
+ *   for every batch b and query head h, with KV head g = h / (Hq / Hkv)
+ *   (grouped-query sharing, same page, Methodology: "GQA with eight heads per
+ *   group", MQA when Hkv = 1):
+ *     s_ij   = scale * sum_d Q[b,h,i,d] * K[b,g,j,d]
+ *     vis_ij = (j < Sk) and (not causal or j <= i + Sk - Sq)   (bottom-right)
+ *     m_i    = max over visible j of s_ij
+ *     e_ij   = exp(s_ij - m_i)            (visible j only)
+ *     l_i    = sum_j e_ij
+ *     O[i,:] = sum_j e_ij * V[b,g,j,:] / l_i
+ *     LSE_i  = m_i + ln(l_i)              (natural log, includes the scale)
+ *   A row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * Decode (same page, Methodology / Evaluation: FlashDecoding -- GEMV plus
+ * softmax, memory bound) is the same definition with Sq = 1, no mask, split
+ * along the key axis: chunk = ceil(Sk / ns), split s covers keys
+ * [s*chunk, min(Sk, (s+1)*chunk)); each split returns its own normalised
+ * O_s and its own LSE_s (empty split: O_s = 0, LSE_s = -inf), and the
+ * combine step returns LSE = ln sum_s exp(LSE_s) and
+ * O = sum_s exp(LSE_s - LSE) * O_s.
+ *
+ * Inputs are bf16 bit patterns (uint16, row-major [B,H,S,D]); each value is
+ * widened exactly to double.  All arithmetic is double, in the order the
+ * definition states; there is no blocking, no online softmax and no
+ * reordering beyond it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Number of visible keys for query row i: the visible set is the prefix
+ * [0, nvis) of the key axis. */
+static int64_t visible_keys(int64_t i, int64_t Sq, int64_t Sk, int causal)
+{
+    if (!causal) return Sk;
+    int64_t n = i + Sk - Sq + 1;
+    if (n < 0) n = 0;
+    if (n > Sk) n = Sk;
+    return n;
+}
+
+/* One query row against keys [j0, j1) of one KV head.
+ * q: D values (double); kh, vh: the KV head's [Sk, D] bf16 matrices.
+ * s: scratch of at least (j1 - j0) doubles. */
+static void attend_row(const double *q, const uint16_t *kh, const uint16_t *vh,
+                       int64_t j0, int64_t j1, int64_t D, double scale,
+                       double *s, double *o, double *lse)
+{
+    int64_t n = j1 - j0;
+    if (n <= 0) {
+        for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    /* scores */
+    for (int64_t j = 0; j < n; ++j) {
+        const uint16_t *kr = kh + (j0 + j) * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d) acc += q[d] * bf16_to_double(kr[d]);
+        s[j] = scale * acc;
+    }
+    /* m = max over visible keys */
+    double m = s[0];
+    for (int64_t j = 1; j < n; ++j)
+        if (s[j] > m) m = s[j];
+    /* e = exp(s - m), l = sum e (e overwrites s) */
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    /* O = sum e * V / l */
+    for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const uint16_t *vr = vh + (j0 + j) * D;
+        double e = s[j];
+        for (int64_t d = 0; d < D; ++d) o[d] += e * bf16_to_double(vr[d]);
+    }
+    for (int64_t d = 0; d < D; ++d) o[d] /= l;
+    *lse = m + log(l);
+}
+
+static int check_dims(int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk,
+                      int64_t D)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return 1;
+    if (Hq % Hkv != 0) return 1;
+    return 0;
+}
+
+/*
+ * Attention forward for a list of query rows.
+ *   rows: flat row ids r = (b*Hq + h)*Sq + i; NULL means every row in order.
+ *   o_out: [nrows, D] doubles; lse_out: [nrows] doubles.
+ * Returns 0 on success, nonzero on invalid arguments.
+ */
+int oracle_attn_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq,
+                         int64_t Sk, int64_t D, int causal, double scale,
+                         const int64_t *rows, int64_t nrows, double *o_out,
+                         double *lse_out)
+{
+    if (check_dims(B, Hq, Hkv, Sq, Sk, D)) return 1;
+    int64_t total = B * Hq * Sq;
+    if (rows == NULL) nrows = total;
+    int64_t group = Hq / Hkv;
+    int bad = 0;
+
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        if (s == NULL || qd == NULL) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < nrows; ++t) {
+                int64_t r = rows ? rows[t] : t;
+                if (r < 0 || r >= total) {
+#pragma omp atomic write
+                    bad = 1;
+                    continue;
+                }
+                int64_t i = r % Sq;
+                int64_t bh = r / Sq;
+                int64_t h = bh % Hq;
+                int64_t b = bh / Hq;
+                int64_t g = h / group;
+                const uint16_t *qr = q + r * D;
+                for (int64_t d = 0; d < D; ++d) qd[d] = bf16_to_double(qr[d]);
+                const uint16_t *kh = k + (b * Hkv + g) * Sk * D;
+                const uint16_t *vh = v + (b * Hkv + g) * Sk * D;
+                int64_t nvis = visible_keys(i, Sq, Sk, causal);
+                attend_row(qd, kh, vh, 0, nvis, D, scale, s, o_out + t * D,
+                           lse_out + t);
+            }
+        }
+        free(s);
+        free(qd);
+    }
+    return bad;
+}
+
+/*
+ * Split-KV decode partials (Sq = 1, no mask).
+ *   q: [B,Hq,1,D]; k, v: [B,Hkv,Sk,D] (bf16 bits).
+ *   o_part: [ns,B,Hq,D]; lse_part: [ns,B,Hq].
+ */
+int oracle_decode_split(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        int64_t B, int64_t Hq, int64_t Hkv, int64_t Sk, int64_t D,
+                        int64_t ns, double scale, double *o_part,
+                        double *lse_part)
+{
+    if (check_dims(B, Hq, Hkv, 1, Sk, D) || ns <= 0) return 1;
+    int64_t group = Hq / Hkv;
+    int64_t chunk = (Sk + ns - 1) / ns;
+    int64_t units = ns * B * Hq;
+    int bad = 0;
+
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(chunk > 0 ? chunk : 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+        if (s == NULL || qd == NULL) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t u = 0; u < units; ++u) {
+                int64_t bh = u % (B * Hq);
+                int64_t sp = u / (B * Hq);
+                int64_t h = bh % Hq;
+                int64_t b = bh / Hq;
+                int64_t g = h / group;
+                const uint16_t *qr = q + bh * D;
+                for (int64_t d = 0; d < D; ++d) qd[d] = bf16_to_double(qr[d]);
+                int64_t j0 = sp * chunk;
+                int64_t j1 = j0 + chunk;
+                if (j0 > Sk) j0 = Sk;
+                if (j1 > Sk) j1 = Sk;
+                const uint16_t *kh = k + (b * Hkv + g) * Sk * D;
+                const uint16_t *vh = v + (b * Hkv + g) * Sk * D;
+                attend_row(qd, kh, vh, j0, j1, D, scale, s, o_part + u * D,
+                           lse_part + u);
+            }
+        }
+        free(s);
+        free(qd);
+    }
+    return bad;
+}
+
+/*
+ * Log-sum-exp combine of ns partials.
+ *   o_part: [ns,R,D]; lse_part: [ns,R] with R = B*Hq rows.
+ *   o: [R,D]; lse: [R].
+ */
+int oracle_combine(const double *o_part, const double *lse_part, int64_t R,
+                   int64_t D, int64_t ns, double *o, double *lse)
+{
+    if (R < 0 || D <= 0 || ns <= 0) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        double M = -INFINITY;
+        for (int64_t sp = 0; sp < ns; ++sp)
+            if (lse_part[sp * R + r] > M) M = lse_part[sp * R + r];
+        for (int64_t d = 0; d < D; ++d) o[r * D + d] = 0.0;
+        if (M == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double W = 0.0;
+        for (int64_t sp = 0; sp < ns; ++sp) W += exp(lse_part[sp * R + r] - M);
+        double L = M + log(W);
+        for (int64_t sp = 0; sp < ns; ++sp) {
+            double w = exp(lse_part[sp * R + r] - L);
+            if (w == 0.0) continue;
+            for (int64_t d = 0; d < D; ++d)
+                o[r * D + d] += w * o_part[(sp * R + r) * D + d];
+        }
+        lse[r] = L;
+    }
+    return 0;
+}
