@@ -1,0 +1,408 @@
+"""Benchmark of the attention forward (prefill) and split-KV decode on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line is printed by rank 0.  ``value`` is the prefill throughput in
+TFLOP/s (counted FLOPs 4*B*Hq*Sq*Sk*D, halved for causal) on the causal GQA
+workload B=2, Hq=32, Hkv=8, S=8192, D=128; a step is one attn_fwd launch with
+its inputs resident in HBM.  L2 is flushed between steps by writing a 256 MiB
+buffer outside the timed events.  The ``decode`` object reports the split-KV
+decode + combine (B=64, Hq=32, Hkv=8, Sk=4096, D=128, 8 splits) in GB/s of
+algorithmic bytes.  ``e2e`` repeats the prefill through the public API with
+pinned host buffers, the host<->device copies inside the timed region.
+
+--impl reference times the fp64 CPU oracle on the same workload (a bounded
+sample of query rows per step) and prints the same line with impl=reference.
+Multi-GPU (torchrun): every rank runs its own replica (replicas only, no
+collective on the data path); value = total FLOPs of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from attn_inputs import WORKLOADS, sample_rows, workload_inputs  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s & % BF16 TC peak (prefill); decode HBM GB/s & % of peak"
+PREFILL = WORKLOADS[3]
+DECODE = WORKLOADS[5]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per launch of the prefill kernel on the workload
+# above, from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`;
+# None until a capture of the current kernel exists (profiles/ holds the summary).
+PREFILL_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while work runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t is not None:
+            self.t.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, line in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_launches(fn, steps, warmup, flush_buf, stream):
+    """Per-step CUDA-event times (ms) of fn() on `stream`, L2 flushed in between."""
+    for _ in range(warmup):
+        flush_l2(flush_buf)
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush_buf)
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def barrier(dist_on):
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dist_on: bool, device) -> float:
+    if not dist_on:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_rows_flops(w, rows):
+    """Counted FLOPs (4*D per visible key) of a set of flat row ids."""
+    i = rows % w.Sq
+    if w.causal:
+        nvis = torch.clamp(i + w.Sk - w.Sq + 1, 0, w.Sk)
+    else:
+        nvis = torch.full_like(i, w.Sk)
+    return float(4.0 * w.D * nvis.double().sum())
+
+
+def run_oracle_sample(w, q, k, v, target_s: float, seed: int = 0):
+    """Time the oracle on a row sample sized to take about target_s seconds."""
+    import oracle  # CPU baseline only
+    n = 64
+    while True:
+        rows = sample_rows(w.B, w.Hq, w.Sq, n_random=n, seed=seed)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w.causal, w.scale, rows=rows.numpy())
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= w.B * w.Hq * w.Sq:
+            return rows, dt
+        n = min(int(n * max(2.0, 1.2 * target_s / max(dt, 1e-3))), w.B * w.Hq * w.Sq)
+
+
+def omp_threads() -> int:
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.isdigit():
+        return int(env)
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+           "D": w.D, "causal": w.causal, "inputs": "bf16 N(0,1) Q/K/V from seed %d" % w.seed,
+           "parallelism": "replicas"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def reference_arm(args, rank, world):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    w = PREFILL
+    q, k, v = workload_inputs(w)
+    total = args.steps + args.warmup
+    per_step = max(0.5, min(10.0, 90.0 / max(1, total)))
+    rows, _ = run_oracle_sample(w, q, k, v, per_step, seed=w.seed)
+    import oracle
+    flops = oracle_rows_flops(w, rows)
+    for _ in range(args.warmup):
+        oracle.attn_fwd(q, k, v, w.causal, w.scale, rows=rows.numpy())
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w.causal, w.scale, rows=rows.numpy())
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = flops / sec / 1e12
+    sample = f"{rows.numel()} query rows of the workload per step ({flops / 1e9:.1f} GFLOP counted)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, {"l2": "n/a (CPU)"}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": omp_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args, rank, world, local_rank, dist_on):
+    import tensor_attn_fwd_gb300 as attn
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream()
+    peaks, peaks_src = load_peaks()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+
+    flush_buf = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=device)  # 256 MiB
+
+    # ---------------- prefill (value)
+    w = PREFILL
+    q_h, k_h, v_h = workload_inputs(w)
+    q, k, v = q_h.to(device), k_h.to(device), v_h.to(device)
+    o = torch.empty((w.B, w.Hq, w.Sq, w.D), dtype=torch.float32, device=device)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
+
+    def prefill():
+        attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse, stream=stream)
+
+    prefill()
+    torch.cuda.synchronize()
+    if attn.attn_debug_status() != attn.ATTN_OK:
+        raise RuntimeError("prefill kernel reported a timeout")
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    t_clock0 = time.time()
+    times = time_launches(prefill, args.steps, args.warmup, flush_buf, stream)
+    torch.cuda.synchronize()
+    barrier(dist_on)
+    t_clock1 = time.time()
+    ms = sum(times) / len(times)
+    ms_max = max_over_ranks(ms, dist_on, device)
+    flops = w.flops()
+    value = flops * world / (ms_max * 1e-3) / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+
+    # ---------------- decode (split-KV + combine)
+    d = DECODE
+    dq_h, dk_h, dv_h = workload_inputs(d)
+    dq, dk, dv = dq_h.to(device), dk_h.to(device), dv_h.to(device)
+    op = torch.empty((d.num_splits, d.B, d.Hq, d.D), dtype=torch.float32, device=device)
+    lp = torch.empty((d.num_splits, d.B, d.Hq), dtype=torch.float32, device=device)
+    do = torch.empty((d.B, d.Hq, d.D), dtype=torch.float32, device=device)
+    dl = torch.empty((d.B, d.Hq), dtype=torch.float32, device=device)
+
+    def decode_split():
+        attn.attn_decode_splitkv(dq, dk, dv, d.num_splits, d.scale, op, lp, stream=stream)
+
+    def decode_combine():
+        attn.attn_combine(op, lp, do, dl, stream=stream)
+
+    def decode_both():
+        decode_split()
+        decode_combine()
+
+    decode_both()
+    torch.cuda.synchronize()
+    t_both = time_launches(decode_both, args.steps, args.warmup, flush_buf, stream)
+    t_split = time_launches(decode_split, args.steps, args.warmup, flush_buf, stream)
+    t_comb = time_launches(decode_combine, args.steps, args.warmup, flush_buf, stream)
+    t_clock2 = time.time()
+    dbytes = d.algorithmic_bytes()
+    d_ms = sum(t_both) / len(t_both)
+    d_split_ms = sum(t_split) / len(t_split)
+    decode = {
+        "workload": d.name, "metric": "decode HBM GB/s (algorithmic bytes)",
+        "value": dbytes / (d_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": d_ms,
+        "split_kernel_ms": d_split_ms, "combine_kernel_ms": sum(t_comb) / len(t_comb),
+        "algorithmic_bytes": dbytes,
+        "frac_of_measured_hbm": dbytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "frac_of_nominal_8tbs": dbytes / (d_ms * 1e-3) / 1e9 / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": dbytes / (d_split_ms * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": dbytes / (d_split_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": DECODE_TRAFFIC_BYTES,
+                     "peak_source": f"{peaks_src} STREAM-style copy"},
+    }
+
+    # ---------------- end to end through the public API, host buffers
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        op_h = torch.empty(o.shape, dtype=torch.float32).pin_memory()
+        lp_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            qd = qp.to(device, non_blocking=True)
+            kd = kp.to(device, non_blocking=True)
+            vd = vp.to(device, non_blocking=True)
+            oo, ll = attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, stream=stream)
+            op_h.copy_(oo, non_blocking=True)
+            lp_h.copy_(ll, non_blocking=True)
+
+        e_steps = max(3, min(args.steps, 10))
+        e_times = time_launches(e2e_step, e_steps, 2, flush_buf, stream)
+        e_ms = max_over_ranks(sum(e_times) / len(e_times), dist_on, device)
+        h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+        d2h = op_h.numel() * 4 + lp_h.numel() * 4
+        e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    sampler.stop()
+    clocks = sampler.summary(t_clock0, t_clock2)
+
+    # ---------------- CPU baseline: the oracle on a bounded row sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows, dt = run_oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds, seed=w.seed)
+        cflops = oracle_rows_flops(w, rows)
+        cpu = {"value": cflops / dt / 1e12, "unit": "TFLOP/s", "cores": omp_threads(),
+               "kind": "oracle",
+               "sample": f"{rows.numel()} query rows of {w.name} ({cflops / 1e9:.1f} GFLOP "
+                         f"counted, {dt:.1f} s)"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(w, {"l2": "flushed between steps (256 MiB write outside "
+                                            "the timed events); inputs+outputs 472 MB > L2"}),
+        "frac_of_measured_bf16_peak": achieved / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": PREFILL_TRAFFIC_BYTES,
+                     "peak_source": f"{peaks_src} cuBLAS bf16 burst"},
+        "decode": decode,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    if dist_on:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        ours_arm(args, rank, world, local_rank, dist_on)
+    finally:
+        if dist_on:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

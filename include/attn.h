@@ -1,0 +1,120 @@
+/*
+ * attn.h -- C ABI of libattn.so, a GB300 (sm_103a) attention-forward library.
+ *
+ * The operation is multi-head scaled-dot-product attention computed in one
+ * fused pass ("A Thread-Register Decoupled GPU Execution Model for Efficient
+ * Tensor Computation", Background, Equ. 1 -- referenced there, not printed;
+ * its standard content is used):
+ *
+ *   S = Q K^T * scale (+ causal mask),  P = softmax(S) row-wise,  O = P V,
+ *   LSE = ln sum_j exp(S_ij)   (natural log, over visible keys, scale included)
+ *
+ * with grouped-query sharing (same page, Methodology: GQA "eight heads per
+ * group" and MQA): query head h reads KV head h / (Hq / Hkv).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE memory owned by the caller.  The library
+ *    never allocates, frees or synchronises on these paths; each call enqueues
+ *    its kernels on `stream` and returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Layout is row-major, contiguous: Q [B,Hq,Sq,D], K and V [B,Hkv,Sk,D]
+ *    (bf16), O [B,Hq,Sq,D] and LSE [B,Hq,Sq] (fp32).
+ *  - The return value is an attn_status.  Arguments are validated before any
+ *    launch; a rejected call launches nothing.  ATTN_ERR_CUDA reports a launch
+ *    failure (cudaGetLastError).  Errors raised asynchronously by a kernel
+ *    surface on the caller's next synchronisation, as in CUDA itself; a kernel
+ *    whose internal wait gave up records ATTN_ERR_TIMEOUT, readable with
+ *    attn_debug_status().
+ *  - Thread safety: calls may be made concurrently from several host threads.
+ */
+#ifndef TENSOR_ATTN_FWD_GB300_ATTN_H
+#define TENSOR_ATTN_FWD_GB300_ATTN_H
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. D not in {64, 128}) */
+    ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+    ATTN_ERR_CUDA = 4,         /* the CUDA runtime reported an error */
+    ATTN_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (device status) */
+} attn_status;
+
+/*
+ * Prefill / general attention forward.
+ * Source: "A Thread-Register Decoupled GPU Execution Model for Efficient
+ * Tensor Computation", Background (Equ. 1; fused FlashAttention-style
+ * computation; softmax phase interleaved with the two GEMMs, Fig. 2) and
+ * Methodology (GQA/MQA).  Causal masking is bottom-right aligned: query row i
+ * sees key j iff j <= i + Sk - Sq.  A row that sees no key gets O = 0 and
+ * LSE = -inf.
+ *
+ *   q  [B,Hq,Sq,D] bf16     k, v [B,Hkv,Sk,D] bf16
+ *   o  [B,Hq,Sq,D] fp32     lse  [B,Hq,Sq]    fp32
+ *   B >= 1, Hq >= 1, Hkv >= 1, Hq % Hkv == 0, Sq >= 1, Sk >= 1, D in {64, 128}
+ *   causal in {0, 1}; scale is applied to QK^T (callers usually pass 1/sqrt(D)).
+ * All pointers must be 16-byte aligned.
+ */
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, float *o, float *lse,
+             int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+             void *stream);
+
+/*
+ * Split-KV decode, first stage: per-split partial results for one query row
+ * per head.  Source: same page, Methodology and Evaluation (FlashDecoding:
+ * decode is GEMV plus softmax, memory bound, no tensor cores).
+ *
+ * The key axis is cut into num_splits chunks of ceil(Sk / num_splits) keys;
+ * split s covers keys [s*chunk, min(Sk, (s+1)*chunk)).  For each split,
+ * o_part holds the split's own normalised output and lse_part its own
+ * log-sum-exp; an empty split writes O = 0 and LSE = -inf.
+ *
+ *   q [B,Hq,1,D] bf16;  k, v [B,Hkv,Sk,D] bf16 (contiguous KV per sequence)
+ *   o_part [num_splits,B,Hq,D] fp32;  lse_part [num_splits,B,Hq] fp32
+ *     (caller-owned workspace, fully overwritten)
+ *   1 <= num_splits <= Sk; D in {64, 128}; no mask.
+ */
+ATTN_API int attn_decode_splitkv(const void *q, const void *k, const void *v, float *o_part,
+                        float *lse_part, int B, int Hq, int Hkv, int Sk, int D,
+                        int num_splits, float scale, void *stream);
+
+/*
+ * Split-KV decode, second stage: log-sum-exp combine of the partials.
+ * Source: same page (FlashDecoding's reduction across key splits).
+ *   lse = ln sum_s exp(lse_s);  o = sum_s exp(lse_s - lse) * o_s
+ * Rows whose splits are all empty get o = 0, lse = -inf.
+ *
+ *   o_part [num_splits,B,Hq,D], lse_part [num_splits,B,Hq] (fp32, as written
+ *   by attn_decode_splitkv);  o [B,Hq,D] fp32;  lse [B,Hq] fp32.
+ */
+ATTN_API int attn_combine(const float *o_part, const float *lse_part, float *o, float *lse, int B,
+                 int Hq, int D, int num_splits, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+ATTN_API const char *attn_status_string(int status);
+
+/*
+ * Debug: synchronise `stream`, then read and clear this device's kernel
+ * status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel's bounded wait
+ * expired since the last read) or ATTN_ERR_CUDA (the synchronisation itself
+ * failed).  Not for the hot path: it blocks the calling thread.
+ */
+ATTN_API int attn_debug_status(void *stream);
+
+/* Library ABI version, (major << 16) | minor. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TENSOR_ATTN_FWD_GB300_ATTN_H */

@@ -1,0 +1,213 @@
+"""Python binding of libattn.so -- a GB300 (sm_103a) attention-forward library.
+
+This module only marshals arguments: it checks dtypes, shapes, contiguity and
+devices, allocates outputs with PyTorch when the caller does not pass them,
+and calls the C ABI declared in ``include/attn.h`` on the current CUDA stream.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback -- if the library is missing or a call fails, an
+exception is raised.
+
+Names follow the C ABI:
+    attn_fwd(q, k, v, causal, scale)            -> (o, lse)
+    attn_decode_splitkv(q, k, v, num_splits)    -> (o_part, lse_part)
+    attn_combine(o_part, lse_part)              -> (o, lse)
+    decode(q, k, v, num_splits)                 -> (o, lse)   both stages
+Layouts: Q [B,Hq,Sq,D], K/V [B,Hkv,Sk,D] bf16; O [B,Hq,Sq,D], LSE [B,Hq,Sq] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = ["AttnError", "attn_fwd", "attn_decode_splitkv", "attn_combine", "decode",
+           "attn_status_string", "attn_debug_status", "library_path", "load_library",
+           "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
+           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libattn.so"
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_flt = ctypes.c_float
+
+# Exported symbols and their C signatures (include/attn.h).
+_SIGNATURES = {
+    "attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _int, _flt,
+                  _vp], _int),
+    "attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
+                             _flt, _vp], _int),
+    "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
+    "attn_status_string": ([_int], ctypes.c_char_p),
+    "attn_debug_status": ([_vp], _int),
+    "attn_version": ([], _int),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        msg = attn_status_string(status)
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def library_path() -> str:
+    return os.path.join(_PKG_DIR, _LIB_NAME)
+
+
+def load_library():
+    """Load libattn.so (built by ``tensor_attn_fwd_gb300.build``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(
+                    f"{path} is missing: build it with `python -m tensor_attn_fwd_gb300.build` "
+                    "(or __graft_entry__.build()); there is no fallback implementation")
+            lib = ctypes.CDLL(path)
+            for name, (argtypes, restype) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = lib
+    return _lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_debug_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status word."""
+    return int(load_library().attn_debug_status(_stream_handle(stream)))
+
+
+def _check(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_bf16(name: str, t: torch.Tensor, ndim: int):
+    _check(isinstance(t, torch.Tensor), f"{name} must be a torch.Tensor")
+    _check(t.is_cuda, f"{name} must be a CUDA tensor")
+    _check(t.dtype == torch.bfloat16, f"{name} must be bfloat16, got {t.dtype}")
+    _check(t.dim() == ndim, f"{name} must have {ndim} dims, got {t.dim()}")
+    _check(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def _out(t, shape, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=torch.float32, device=device)
+    _check(t.is_cuda and t.dtype == torch.float32 and t.is_contiguous(),
+           f"{name} must be a contiguous float32 CUDA tensor")
+    _check(tuple(t.shape) == tuple(shape), f"{name} must have shape {tuple(shape)}")
+    _check(t.device == device, f"{name} must be on {device}")
+    return t
+
+
+def _raise_if(status: int, what: str):
+    if status != ATTN_OK:
+        raise AttnError(status, what)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: float | None = None, o: torch.Tensor | None = None,
+             lse: torch.Tensor | None = None, stream=None):
+    """Attention forward: O = softmax(Q K^T * scale (+ causal mask)) V and its LSE.
+
+    q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] (bf16, contiguous, same device).
+    Returns (o [B,Hq,Sq,D] fp32, lse [B,Hq,Sq] fp32).
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(k.device == q.device and v.device == q.device, "q/k/v must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = _out(o, (B, Hq, Sq, D), q.device, "o")
+    lse = _out(lse, (B, Hq, Sq), q.device, "lse")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
+                          float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_fwd")
+    return o, lse
+
+
+def attn_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
+                        scale: float | None = None, o_part: torch.Tensor | None = None,
+                        lse_part: torch.Tensor | None = None, stream=None):
+    """Split-KV decode partials for q [B,Hq,1,D] against k/v [B,Hkv,Sk,D].
+
+    Returns (o_part [num_splits,B,Hq,D], lse_part [num_splits,B,Hq]) fp32.
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    _check(Sq == 1, "decode takes one query row per head (q.shape[2] == 1)")
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(k.device == q.device and v.device == q.device, "q/k/v must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ns = int(num_splits)
+    o_part = _out(o_part, (ns, B, Hq, D), q.device, "o_part")
+    lse_part = _out(lse_part, (ns, B, Hq), q.device, "lse_part")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     o_part.data_ptr(), lse_part.data_ptr(), B, Hq, Hkv, Sk, D,
+                                     ns, float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_decode_splitkv")
+    return o_part, lse_part
+
+
+def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, stream=None):
+    """LSE combine: o_part [ns,B,Hq,D], lse_part [ns,B,Hq] -> (o [B,Hq,D], lse [B,Hq])."""
+    _check(o_part.is_cuda and o_part.dtype == torch.float32 and o_part.is_contiguous()
+           and o_part.dim() == 4, "o_part must be a contiguous [ns,B,Hq,D] float32 CUDA tensor")
+    ns, B, Hq, D = o_part.shape
+    _check(lse_part.is_cuda and lse_part.dtype == torch.float32 and lse_part.is_contiguous()
+           and tuple(lse_part.shape) == (ns, B, Hq), "lse_part must be [ns,B,Hq] float32")
+    o = _out(o, (B, Hq, D), o_part.device, "o")
+    lse = _out(lse, (B, Hq), o_part.device, "lse")
+    lib = load_library()
+    with torch.cuda.device(o_part.device):
+        st = lib.attn_combine(o_part.data_ptr(), lse_part.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, Hq, D, ns, _stream_handle(stream))
+    _raise_if(st, "attn_combine")
+    return o, lse
+
+
+def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
+           scale: float | None = None, workspace=None, o=None, lse=None, stream=None):
+    """Split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq])."""
+    o_part, lse_part = (None, None) if workspace is None else workspace
+    o_part, lse_part = attn_decode_splitkv(q, k, v, num_splits, scale, o_part, lse_part, stream)
+    return attn_combine(o_part, lse_part, o, lse, stream)

@@ -1,0 +1,191 @@
+// api.cu -- the C ABI of libattn.so: argument validation, status codes and the
+// per-device state (SM count, kernel attributes, device status word).  Every
+// entry point validates before launching; nothing here allocates device
+// memory or synchronises, except attn_debug_status().
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Written by kernels whose bounded wait expired (ATTN_ERR_TIMEOUT).
+__device__ int g_status_word = 0;
+
+std::mutex g_mutex;
+int g_sm_count[kMaxDevices] = {0};
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+struct AttrEntry {
+  const void* kernel;
+  int bytes;
+  uint64_t device_mask;
+};
+AttrEntry g_attr[16];
+int g_attr_n = 0;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sizes are int on the ABI; keep every product the kernels form in range.
+constexpr long long kMaxElems = 1ll << 40;
+constexpr int kMaxSeq = 1 << 30;
+
+}  // namespace
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int* status_word_device_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  AttrEntry* e = nullptr;
+  for (int i = 0; i < g_attr_n; ++i)
+    if (g_attr[i].kernel == kernel) e = &g_attr[i];
+  if (e != nullptr && e->bytes >= bytes && (e->device_mask >> dev & 1u)) return cudaSuccess;
+  const cudaError_t err =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err != cudaSuccess) return err;
+  if (e == nullptr) {
+    if (g_attr_n >= 16) return cudaSuccess;  // table full: set again next time
+    e = &g_attr[g_attr_n++];
+    e->kernel = kernel;
+    e->bytes = bytes;
+    e->device_mask = 0;
+  }
+  e->bytes = bytes;
+  e->device_mask |= uint64_t(1) << dev;
+  return cudaSuccess;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA runtime error";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait expired";
+    default: return "unknown attn status";
+  }
+}
+
+int attn_version(void) { return (1 << 16) | 0; }
+
+int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Sq > kMaxSeq || Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * Sq * D > kMaxElems ||
+      static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
+    return ATTN_ERR_UNSUPPORTED;
+  // Work items (B*Hq*ceil(Sq/256)) are indexed with int.
+  if (static_cast<long long>(B) * Hq * ((Sq + 255) / 256) > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const cudaError_t e = launch_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale,
+                                        static_cast<cudaStream_t>(stream), status);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
+                        float* lse_part, int B, int Hq, int Hkv, int Sk, int D, int num_splits,
+                        float scale, void* stream) {
+  if (!q || !k || !v || !o_part || !lse_part) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > Sk) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv * Sk * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
+  const int head_slices = (Hq / Hkv + 3) / 4;
+  if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
+      !aligned16(lse_part))
+    return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const cudaError_t e =
+      launch_decode_splitkv(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
+                            static_cast<cudaStream_t>(stream), status);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_combine(const float* o_part, const float* lse_part, float* o, float* lse, int B, int Hq,
+                 int D, int num_splits, void* stream) {
+  if (!o_part || !lse_part || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || D <= 0 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems ||
+      static_cast<long long>(B) * Hq > (1ll << 30))
+    return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_MISALIGNED;
+  const cudaError_t e = launch_combine(o_part, lse_part, o, lse, B * Hq, D, num_splits,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_debug_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpyFromSymbol(&value, g_status_word, sizeof(int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return value;
+}
+
+}  // extern "C"

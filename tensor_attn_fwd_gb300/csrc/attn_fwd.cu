@@ -1,0 +1,576 @@
+// attn_fwd.cu -- fused one-pass attention forward on sm_103a tensor cores.
+//
+// Source: "A Thread-Register Decoupled GPU Execution Model for Efficient Tensor
+// Computation": Background (Equ. 1, fused FlashAttention-style attention; the
+// softmax phase -- row max, exp, row sum, rescale -- runs on the SIMD/SFU pipes
+// between the two GEMMs; warp specialisation with mbarrier producer/consumer
+// synchronisation; Blackwell's tensor cores take operands from shared and
+// tensor memory instead of registers, Fig. 2) and Methodology (GQA/MQA).
+//
+// Work item: two 128-row query tiles (256 rows) of one (batch, query head).
+// One persistent CTA per SM walks a static longest-first list of items.
+//
+// Roles (384 threads):
+//   warps 0-3  softmax for query tile 0  (thread r owns TMEM lane / row r)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warp  9    TMA producer (one thread): Q tiles and a K/V stage ring
+//   warps 10-11 idle
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   S_0 [0,128)  S_1 [128,256)  O_0 [256,256+D)  O_1 [256+D,256+2D)
+//   P_t (bf16, two per column) overwrites the first 64 columns of S_t.
+//
+// Per KV tile j and query tile t the MMA warp issues S_t(j) (smem x smem),
+// waits for the softmax warps to turn S_t(j) into P_t(j), then issues
+// O_t += P_t(j) V_j (tmem x smem) followed by S_t(j+1).  While the softmax
+// warps of one tile work, the tensor core runs the other tile's GEMMs.
+// tcgen05 operations issued by one thread execute in order, so S_t(j+1) never
+// overwrites P_t(j) before O_t += P_t(j) V_j has read it.
+//
+// Online softmax (per row, log2 domain, x = s * scale * log2 e):
+//   m' = max(m, max_j x_j); p_j = 2^(x_j - m'); l = l * 2^(m - m') + sum p_j.
+// The rescale of O and l is lazy: the running maximum is only moved (and O
+// rescaled in TMEM) when the new maximum exceeds it by more than 8, so p stays
+// below 2^8; O and l always share the same reference maximum, which keeps the
+// result exact up to rounding.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 384;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kRowsPerItem = 256;
+constexpr uint32_t kSubBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled sub-tile
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kSub = D / 64;
+  static constexpr uint32_t kTileBytes = kSub * kSubBytes;  // 128 x D bf16
+  static constexpr int kStages = (D == 128) ? 5 : 9;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kBarBytes = 256;
+  static constexpr size_t kSmemBytes =
+      1024 + 2 * size_t(kTileBytes) + size_t(kStages) * kTileBytes + kBarBytes;
+  // MMA instruction descriptors.
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+};
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[10], kv_empty[10];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block too large");
+
+struct FwdParams {
+  float* o;
+  float* lse;
+  int* status;
+  int B, Hq, Hkv, Sq, Sk;
+  int causal;
+  float scale_log2;  // scale * log2(e)
+  int num_pairs;     // ceil(Sq / 256)
+  int total_items;   // B * Hq * num_pairs
+};
+
+struct Item {
+  int bh;      // b * Hq + h
+  int q_row0;  // first query row of tile 0
+  int n[2];    // KV tiles needed by query tile 0 / 1 (0: nothing to compute)
+};
+
+// Number of leading keys that query tile t of an item needs, in KV tiles.
+__device__ __forceinline__ int tile_kv_count(const FwdParams& p, int row_first) {
+  if (row_first >= p.Sq) return 0;
+  int nvis = p.Sk;
+  if (p.causal) {
+    const int row_last = min(row_first + 127, p.Sq - 1);
+    nvis = min(p.Sk, row_last + p.Sk - p.Sq + 1);
+    if (nvis <= 0) return 0;
+  }
+  return (nvis + 127) / 128;
+}
+
+// Items are ordered longest first (highest query rows first under the causal
+// mask); CTA c takes indices c, 2G-1-c, 2G+c, ... (boustrophedon), which
+// balances the per-CTA totals of a descending cost list.
+__device__ __forceinline__ int item_index(int round, int cta, int grid) {
+  return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ Item get_item(const FwdParams& p, int idx) {
+  const int BH = p.B * p.Hq;
+  Item it;
+  const int pair = p.num_pairs - 1 - idx / BH;
+  it.bh = idx % BH;
+  it.q_row0 = pair * kRowsPerItem;
+  it.n[0] = tile_kv_count(p, it.q_row0);
+  it.n[1] = tile_kv_count(p, it.q_row0 + 128);
+  return it;
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&bars->abort)) return false;
+    if (globaltimer() - t0 > ATTN_WAIT_NS) {
+      *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                          const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* bars) {
+  using C = Cfg<D>;
+  const int group = p.Hq / p.Hkv;
+  uint32_t kv_ctr = 0, q_ctr = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r, blockIdx.x, gridDim.x);
+    if (idx >= p.total_items) break;
+    const Item it = get_item(p, idx);
+    const int n = max(it.n[0], it.n[1]);
+    if (n == 0) continue;
+    const int b = it.bh / p.Hq, h = it.bh % p.Hq;
+    const int bkv = b * p.Hkv + h / group;
+    if (q_ctr > 0 && !(ok = wait_or_abort(&bars->q_empty, (q_ctr - 1) & 1, bars))) break;
+    mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int s = 0; s < C::kSub; ++s)
+        tma_load_3d(sQ + t * C::kTileBytes + s * kSubBytes, tmQ, &bars->q_full, s * 64,
+                    it.q_row0 + 128 * t, it.bh);
+    ++q_ctr;
+    for (int j = 0; j < n && ok; ++j) {
+#pragma unroll 1
+      for (int kind = 0; kind < 2; ++kind) {
+        const uint32_t st = kv_ctr % C::kStages;
+        if (kv_ctr >= uint32_t(C::kStages) &&
+            !(ok = wait_or_abort(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars)))
+          break;
+        mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
+        const CUtensorMap* map = kind ? tmV : tmK;
+#pragma unroll
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, map, &bars->kv_full[st], s * 64,
+                      j * 128, bkv);
+        ++kv_ctr;
+      }
+    }
+  }
+  if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
+  // Let every copy this thread issued land before the CTA can exit.
+  const uint32_t last = kv_ctr;
+  for (uint32_t c = (last > uint32_t(C::kStages) ? last - C::kStages : 0); c < last; ++c)
+    (void)mbar_wait(&bars->kv_full[c % C::kStages], (c / C::kStages) & 1);
+  if (q_ctr > 0) (void)mbar_wait(&bars->q_full, (q_ctr - 1) & 1);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* bars,
+                         uint32_t tmem) {
+  using C = Cfg<D>;
+  const uint32_t q_addr = smem_u32(sQ);
+  const uint32_t kv_addr = smem_u32(sKV);
+  const uint32_t colS[2] = {C::kColS0, C::kColS1};
+  const uint32_t colO[2] = {C::kColO0, C::kColO1};
+  uint32_t kv_ctr = 0, q_ctr = 0;
+  uint32_t p_phase[2] = {0, 0};
+  bool ok = true;
+
+  // S_t = Q_t K^T over D in steps of 16 (K-major operands, 128B swizzle).
+  auto issue_s = [&](int t, uint32_t kst) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+      const uint64_t a = sdesc_sw128(q_addr + t * C::kTileBytes + off, 16, 1024);
+      const uint64_t bdesc = sdesc_sw128(kv_addr + kst * C::kTileBytes + off, 16, 1024);
+      mma_ss(tmem + colS[t], a, bdesc, C::kIdescQK, kk > 0 ? 1u : 0u);
+    }
+  };
+  // O_t (+)= P_t V over 128 keys in steps of 16 (P from TMEM, V MN-major).
+  auto issue_pv = [&](int t, uint32_t vst, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t bdesc = sdesc_sw128(kv_addr + vst * C::kTileBytes + kk * 2048, kSubBytes, 1024);
+      mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, bdesc, C::kIdescPV,
+             (accumulate || kk > 0) ? 1u : 0u);
+    }
+  };
+  auto acquire_kv = [&](uint32_t& st) -> bool {
+    st = kv_ctr % C::kStages;
+    if (!wait_or_abort(&bars->kv_full[st], (kv_ctr / C::kStages) & 1, bars)) return false;
+    ++kv_ctr;
+    tc_fence_after();
+    return true;
+  };
+
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r, blockIdx.x, gridDim.x);
+    if (idx >= p.total_items) break;
+    const Item it = get_item(p, idx);
+    const int n = max(it.n[0], it.n[1]);
+    if (n == 0) continue;
+    if (!(ok = wait_or_abort(&bars->q_full, q_ctr & 1, bars))) break;
+    ++q_ctr;
+    tc_fence_after();
+
+    uint32_t kst;
+    if (!(ok = acquire_kv(kst))) break;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (it.n[t] > 0) {
+        issue_s(t, kst);
+        tc_commit(&bars->s_full[t]);
+      }
+    }
+    tc_commit(&bars->kv_empty[kst]);
+
+    for (int j = 0; j < n && ok; ++j) {
+      uint32_t vst;
+      if (!(ok = acquire_kv(vst))) break;
+      uint32_t nkst = 0;
+      bool have_next = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (j >= it.n[t]) continue;
+        if (!(ok = wait_or_abort(&bars->p_full[t], p_phase[t], bars))) break;
+        p_phase[t] ^= 1;
+        tc_fence_after();
+        issue_pv(t, vst, j > 0);
+        if (j == it.n[t] - 1) {
+          tc_commit(&bars->o_full[t]);
+        } else {
+          if (!have_next) {
+            if (!(ok = acquire_kv(nkst))) break;
+            have_next = true;
+          }
+          issue_s(t, nkst);
+          tc_commit(&bars->s_full[t]);
+        }
+      }
+      if (!ok) break;
+      tc_commit(&bars->kv_empty[vst]);
+      if (j + 1 < n) {
+        if (!have_next) {
+          if (!(ok = acquire_kv(nkst))) break;
+          have_next = true;
+        }
+        tc_commit(&bars->kv_empty[nkst]);
+      }
+    }
+    if (!ok) break;
+    tc_commit(&bars->q_empty);
+  }
+  if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
+  // Every MMA this thread issued must finish before TMEM is released.
+  tc_commit(&bars->mma_done);
+  (void)mbar_wait(&bars->mma_done, 0);
+}
+
+// ------------------------------------------------------------------ softmax
+template <int D>
+__device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int warp, int lane) {
+  using C = Cfg<D>;
+  const int t = warp >> 2;
+  const int quad = warp & 3;
+  const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t tS = tmem + lane_addr + (t ? C::kColS1 : C::kColS0);
+  const uint32_t tO = tmem + lane_addr + (t ? C::kColO1 : C::kColO0);
+  const float sl2 = p.scale_log2;
+  uint32_t s_phase = 0, o_phase = 0;
+  bool ok = true;
+
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r, blockIdx.x, gridDim.x);
+    if (idx >= p.total_items) break;
+    const Item it = get_item(p, idx);
+    const int nt = it.n[t];
+    const int row = it.q_row0 + 128 * t + quad * 32 + lane;
+    const bool row_valid = row < p.Sq;
+    float* o_row = p.o + (static_cast<size_t>(it.bh) * p.Sq + row) * D;
+    float* lse_ptr = p.lse + static_cast<size_t>(it.bh) * p.Sq + row;
+    if (nt == 0) {
+      // No key visible to any row of this tile (or the tile is past Sq).
+      if (row_valid) {
+#pragma unroll 4
+        for (int c = 0; c < D; c += 4)
+          *reinterpret_cast<float4*>(o_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *lse_ptr = -INFINITY;
+      }
+      continue;
+    }
+    // Largest key index this row may see.
+    const int limit = p.causal ? min(row + p.Sk - p.Sq, p.Sk - 1) : p.Sk - 1;
+    float m = -INFINITY;  // reference maximum (log2 domain)
+    float l = 0.f;
+
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[t], s_phase, bars));
+      if (!ok) break;
+      s_phase ^= 1;
+      tc_fence_after();
+
+      uint32_t sr[128];
+      tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+      tmem_ld64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+      float* s = reinterpret_cast<float*>(sr);
+
+      const int key0 = j * 128;
+      if (__any_sync(0xffffffffu, key0 + 127 > limit)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (key0 + c > limit) s[c] = -INFINITY;
+      }
+      // Row maximum with 8 independent chains (a single chain would serialise
+      // 127 dependent max operations).
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
+#pragma unroll
+      for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w]);
+      const float m_tile = mx8[0] * sl2;
+
+      bool rescale = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m = m_tile;
+      } else if (m_tile - m > kRescaleThreshold) {  // false when both are -inf
+        alpha = ex2(m - m_tile);
+        m = m_tile;
+        l *= alpha;
+        rescale = true;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O_t(j-1) is complete: S_t(j) was committed after O_t += P_t(j-1) V.
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t orow[32];
+          tmem_ld32(tO + c, orow);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
+          tmem_st32(tO + c, orow);
+        }
+      }
+      const float base = (m == -INFINITY) ? 0.f : m;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(s[32 * c + 2 * e], sl2, -base));
+          const float p1 = ex2(fmaf(s[32 * c + 2 * e + 1], sl2, -base));
+          rs[e & 3] += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+    }
+    if (!ok) break;
+
+    // Epilogue: O = O / l, LSE = ln 2 * (m + log2 l).
+    ok = __all_sync(0xffffffffu, wait_or_abort(&bars->o_full[t], o_phase, bars));
+    if (!ok) break;
+    o_phase ^= 1;
+    tc_fence_after();
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t orow[32];
+      tmem_ld32(tO + c, orow);
+      if (row_valid) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(o_row + c + e) =
+              make_float4(__uint_as_float(orow[e]) * inv_l, __uint_as_float(orow[e + 1]) * inv_l,
+                          __uint_as_float(orow[e + 2]) * inv_l, __uint_as_float(orow[e + 3]) * inv_l);
+      }
+    }
+    if (row_valid) *lse_ptr = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  }
+  if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + 2 * C::kTileBytes;
+  Bars* bars = reinterpret_cast<Bars*>(sKV + C::kStages * C::kTileBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_full[t], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 8) {
+    softmax_role<D>(p, bars, tmem, warp, lane);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role<D>(p, sQ, sKV, bars, tmem);
+  } else if (warp == kLoadWarp) {
+    if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [planes, rows, D] bf16 tensor, boxes of [1, 128, 64] with 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* base, int D, int rows, int planes) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(rows), cuuint64_t(planes)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(D) * 2 * cuuint64_t(rows)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Sq, int Sk, int causal, float scale,
+                            cudaStream_t stream, int* status) {
+  using C = Cfg<D>;
+  CUtensorMap tmQ, tmK, tmV;
+  if (!encode_map(&tmQ, q, D, Sq, B * Hq) || !encode_map(&tmK, k, D, Sk, B * Hkv) ||
+      !encode_map(&tmV, v, D, Sk, B * Hkv))
+    return cudaErrorInvalidValue;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<D>),
+                                   static_cast<int>(C::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_pairs = (Sq + kRowsPerItem - 1) / kRowsPerItem;
+  p.total_items = B * Hq * p.num_pairs;
+  const int grid = p.total_items < sm_count() ? p.total_items : sm_count();
+  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                            float scale, cudaStream_t stream, int* status) {
+  if (D == 128)
+    return launch_fwd_impl<128>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream,
+                                status);
+  return launch_fwd_impl<64>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream, status);
+}
+
+}  // namespace attn

@@ -1,0 +1,36 @@
+// internal.h -- declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Device address of the library's status word on the current device (the
+// word kernels write ATTN_ERR_TIMEOUT into).  nullptr on failure.
+int* status_word_device_ptr();
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Raise the kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+// Kernel launchers; arguments are already validated.  Return cudaError_t of
+// the launch.
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                            float scale, cudaStream_t stream, int* status);
+
+cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
+                                  float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
+                                  int num_splits, float scale, cudaStream_t stream,
+                                  int* status);
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,
+                           int rows, int D, int num_splits, cudaStream_t stream);
+
+}  // namespace attn

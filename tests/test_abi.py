@@ -1,0 +1,128 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/attn.h declares, and rejects invalid arguments with the
+documented status before touching the device (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_attn_fwd_gb300 as attn
+from tensor_attn_fwd_gb300 import build as attn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    attn_build.build()
+    return attn.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = set(declared_symbols())
+    assert {"attn_fwd", "attn_decode_splitkv", "attn_combine", "attn_status_string",
+            "attn_debug_status", "attn_version"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = attn.attn_status_string(code)
+        assert s and isinstance(s, str)
+    assert "unknown" in attn.attn_status_string(99)
+    assert lib.attn_version() >> 16 == 1
+
+
+# Fake, never-dereferenced device addresses: validation fails before any launch.
+A = 0x10000000       # 16-byte aligned
+M = 0x10000004       # misaligned
+
+
+def fwd(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=1, Sq=8, Sk=8, D=64, causal=0,
+        scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, None)
+
+
+def dec(lib, q=A, k=A, v=A, op=A, lp=A, B=1, Hq=4, Hkv=1, Sk=64, D=128, ns=4, scale=0.1):
+    return lib.attn_decode_splitkv(q, k, v, op, lp, B, Hq, Hkv, Sk, D, ns, scale, None)
+
+
+def comb(lib, op=A, lp=A, o=A, lse=A, B=1, Hq=4, D=128, ns=4):
+    return lib.attn_combine(op, lp, o, lse, B, Hq, D, ns, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sk=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Sq=(1 << 30) + 1), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(v=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(lse=M), attn.ATTN_ERR_MISALIGNED),
+])
+def test_fwd_rejects(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(op=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=65), attn.ATTN_ERR_INVALID_ARG),   # more splits than keys
+    (dict(Hq=6, Hkv=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=70000), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(k=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(lp=M), attn.ATTN_ERR_MISALIGNED),
+])
+def test_decode_rejects(lib, kw, code):
+    assert dec(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(op=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(o=M), attn.ATTN_ERR_MISALIGNED),
+])
+def test_combine_rejects(lib, kw, code):
+    assert comb(lib, **kw) == code
+
+
+def test_python_binding_checks_without_gpu():
+    import torch
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)  # CPU tensors are rejected before any call
+
+
+def test_binding_has_no_fallback_import():
+    # The product binding must not reach the oracle.
+    src = open(os.path.join(ROOT, "tensor_attn_fwd_gb300", "__init__.py")).read()
+    assert "oracle" not in src.replace("no CPU or PyTorch fallback", "")
