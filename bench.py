@@ -372,6 +372,33 @@ def ours_arm(args, rank, world, local_rank, dist_on):
     print(json.dumps(line), flush=True)
 
 
+def profile_arm(args):
+    """A short run of one kernel for ncu: `--profile prefill|decode`, no flush,
+    no e2e, no CPU baseline; `--batch` shrinks the workload's batch."""
+    import dataclasses
+
+    import tensor_attn_fwd_gb300 as attn
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = PREFILL if args.profile == "prefill" else DECODE
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
+    q, k, v = (t.to(device) for t in workload_inputs(w))
+    if args.profile == "prefill":
+        def fn():
+            attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    else:
+        def fn():
+            attn.decode(q, k, v, w.num_splits, w.scale)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    if attn.attn_debug_status() != attn.ATTN_OK:
+        raise RuntimeError("kernel reported a timeout")
+    print(json.dumps({"profile": args.profile, "workload": w.describe(),
+                      "launches": args.warmup + args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -381,8 +408,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="run a few launches of one kernel (for ncu) and exit")
+    ap.add_argument("--batch", type=int, default=0, help="override B in --profile mode")
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be >= 3")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -391,6 +421,9 @@ def main():
     dist_on = world > 1
     if args.impl == "reference":
         reference_arm(args, rank, world)
+        return
+    if args.profile:
+        profile_arm(args)
         return
     if dist_on:
         import torch.distributed as dist
