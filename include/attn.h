@@ -113,6 +113,42 @@ ATTN_API int attn_debug_status(void *stream);
 /* Library ABI version, (major << 16) | minor. */
 ATTN_API int attn_version(void);
 
+/*
+ * Split-KV decode and LSE combine in one call that allocates nothing.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory when they call in -- for example a
+ * plug-in run by a host framework that owns all device memory and gives the
+ * plug-in no allocator, or a latency-critical serving loop that may not call
+ * cudaMalloc/cudaFree (which can synchronise the whole device).  Such callers
+ * cannot supply the o_part/lse_part workspace that attn_decode_splitkv needs.
+ *
+ * Computes exactly what attn_decode_splitkv followed by attn_combine compute
+ * (same arguments, same layouts, same results), but keeps the per-split
+ * partials in a fixed scratch array that is part of the library's own device
+ * image: ATTN_NOALLOC_SCRATCH_FLOATS floats (16 MiB), reserved on every GPU
+ * that loads the library until the process exits.
+ *
+ *   q [B,Hq,1,D] bf16; k, v [B,Hkv,Sk,D] bf16; o [B,Hq,D] fp32; lse [B,Hq] fp32
+ *   (caller-owned device memory, 16-byte aligned).
+ *   Requires num_splits * B * Hq * (D + 1) <= ATTN_NOALLOC_SCRATCH_FLOATS;
+ *   larger requests return ATTN_ERR_UNSUPPORTED and launch nothing.
+ *   Other argument errors are reported as for attn_decode_splitkv.
+ *
+ * Set-up: the first call on a device looks up that device's address of the
+ * scratch array (cudaGetSymbolAddress, no allocation) with the device current;
+ * make that first call before any stream capture.  No call ever allocates or
+ * frees device memory.
+ * Sharing: every call on a device uses the same scratch array, and the array
+ * keeps the last call's partials.  Nothing needs to start at zero -- each call
+ * overwrites every partial it reads -- but calls whose kernels overlap on the
+ * GPU (different streams, or different host threads) race on the array and
+ * must be serialised by the caller, e.g. by issuing them on one stream.
+ */
+#define ATTN_NOALLOC_SCRATCH_FLOATS (4u * 1024u * 1024u)
+ATTN_API int attn_decode_noalloc(const void *q, const void *k, const void *v, float *o,
+                                 float *lse, int B, int Hq, int Hkv, int Sk, int D,
+                                 int num_splits, float scale, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -460,3 +460,78 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o,
 }
 
 }  // namespace attn
+
+// ---------------------------------------------------------------------------
+// attn_decode_noalloc: the decode above with its partials kept in a static
+// device array instead of caller-supplied workspace, for callers that cannot
+// allocate device memory when they call in.  The kernels are the same; only
+// where the partials live differs.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace attn {
+namespace {
+
+// Scratch for the per-split partials: o_part [ns,B,Hq,D] then lse_part
+// [ns,B,Hq].  Part of the module image, so every device that loads the
+// library reserves it until the process exits.  In host code this name is
+// only a host-side stand-in: kernels get the device address looked up below.
+static __device__ __align__(256) float g_decode_scratch[ATTN_NOALLOC_SCRATCH_FLOATS];
+
+constexpr int kScratchMaxDevices = 64;
+std::mutex g_scratch_mutex;
+float* g_scratch_dev_ptr[kScratchMaxDevices] = {nullptr};
+
+// Device address of g_decode_scratch on the current device, looked up once
+// per device (with that device current) and cached.  nullptr on failure.
+float* decode_scratch_ptr() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_dev_ptr[dev] == nullptr) {
+    float* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_decode_scratch) != cudaSuccess)
+      return nullptr;
+    g_scratch_dev_ptr[dev] = p;
+  }
+  return g_scratch_dev_ptr[dev];
+}
+
+bool aligned16_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_decode_noalloc(const void* q, const void* k, const void* v, float* o,
+                                   float* lse, int B, int Hq, int Hkv, int Sk, int D,
+                                   int num_splits, float scale, void* stream) {
+  using namespace attn;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > Sk) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv * Sk * D > (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
+  const int head_slices = (Hq / Hkv + 3) / 4;
+  if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535) return ATTN_ERR_UNSUPPORTED;
+  // The partials must fit the static scratch array.
+  const long long part_floats = static_cast<long long>(num_splits) * B * Hq * D;
+  const long long lse_floats = static_cast<long long>(num_splits) * B * Hq;
+  if (part_floats + lse_floats > static_cast<long long>(ATTN_NOALLOC_SCRATCH_FLOATS))
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16_ptr(q) || !aligned16_ptr(k) || !aligned16_ptr(v) || !aligned16_ptr(o) ||
+      !aligned16_ptr(lse))
+    return ATTN_ERR_MISALIGNED;
+  float* scratch = decode_scratch_ptr();
+  int* status = status_word_device_ptr();
+  if (scratch == nullptr || status == nullptr) return ATTN_ERR_CUDA;
+  float* o_part = scratch;                // D is a multiple of 64: lse_part stays 256-byte aligned
+  float* lse_part = scratch + part_floats;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_splitkv(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits,
+                                        scale, s, status);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = launch_combine(o_part, lse_part, o, lse, B * Hq, D, num_splits, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
