@@ -11,6 +11,7 @@ from __future__ import annotations
 import argparse
 import glob
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -56,12 +57,40 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
+# Kernels that rebalance registers with setmaxnreg must be compiled with exactly
+# the per-thread count their split assumes (threads x count = the pool that
+# setmaxnreg.inc draws from); a smaller count would make .inc wait forever.
+EXACT_REGISTERS = {"attn_fwd_kernel": 168}
+
+
+def check_register_counts(ptxas_log: str):
+    """Parse `ptxas -v` output; raise if a kernel in EXACT_REGISTERS deviates."""
+    current = None
+    seen = set()
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            for name, want in EXACT_REGISTERS.items():
+                if name in current:
+                    seen.add(name)
+                    if int(m.group(1)) != want:
+                        raise RuntimeError(
+                            f"{current}: ptxas used {m.group(1)} registers, the setmaxnreg "
+                            f"split needs exactly {want}")
+            current = None
+    return seen
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + list(extra_flags or [])
+    flags = NVCC_FLAGS + ["-Xptxas", "-v"] + list(extra_flags or [])
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
@@ -72,14 +101,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     with ThreadPoolExecutor(max_workers=max(1, min(len(sources()), os.cpu_count() or 1))) as ex:
         results = list(ex.map(compile_one, sources()))
     failed = False
+    seen = set()
     for src, _, r in results:
         if verbose or r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode != 0:
             failed = True
             sys.stderr.write(f"nvcc failed for {src}\n")
+        else:
+            seen |= check_register_counts(r.stdout + r.stderr)
     if failed:
         raise RuntimeError("libattn build failed")
+    missing = set(EXACT_REGISTERS) - seen
+    if missing:
+        raise RuntimeError(f"no ptxas register report for {sorted(missing)}")
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *[o for _, o, _ in results],
            "-o", tmp]

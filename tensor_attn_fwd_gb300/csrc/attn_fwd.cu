@@ -56,6 +56,11 @@ constexpr int kLoadWarp = 9;
 constexpr int kRowsPerItem = 256;
 constexpr uint32_t kSubBytes = 128 * 128;  // one [128 rows x 64 bf16] swizzled sub-tile
 constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 104;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kLaunchRegs,
+              "register split must use exactly the launch allocation");
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
@@ -77,7 +82,7 @@ struct Cfg {
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[10], kv_empty[10];
-  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t s_full[2], p_full[2][2], o_full[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -207,38 +212,58 @@ template <int D>
 __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* bars,
                          uint32_t tmem) {
   using C = Cfg<D>;
-  const uint32_t q_addr = smem_u32(sQ);
-  const uint32_t kv_addr = smem_u32(sKV);
-  const uint32_t colS[2] = {C::kColS0, C::kColS1};
-  const uint32_t colO[2] = {C::kColO0, C::kColO1};
+  // Descriptor words: the high word is fixed per operand kind, the low word is
+  // (smem address >> 4) plus the leading-byte-offset field, so each MMA only
+  // adds a compile-time offset to a base.
+  constexpr uint64_t kDescK = sdesc_sw128(0, 16, 1024);         // Q and K: K-major
+  constexpr uint64_t kDescV = sdesc_sw128(0, kSubBytes, 1024);  // V: MN-major
+  constexpr uint32_t kHi = static_cast<uint32_t>(kDescK >> 32);
+  static_assert(static_cast<uint32_t>(kDescV >> 32) == kHi, "same SBO/swizzle words");
+  constexpr uint32_t kLoK = static_cast<uint32_t>(kDescK);
+  constexpr uint32_t kLoV = static_cast<uint32_t>(kDescV);
+  constexpr uint32_t kTile16 = C::kTileBytes >> 4;
+  const uint32_t q_lo = kLoK + (smem_u32(sQ) >> 4);
+  const uint32_t k_lo = kLoK + (smem_u32(sKV) >> 4);
+  const uint32_t v_lo = kLoV + (smem_u32(sKV) >> 4);
   uint32_t kv_ctr = 0, q_ctr = 0;
   uint32_t p_phase[2] = {0, 0};
   bool ok = true;
 
   // S_t = Q_t K^T over D in steps of 16 (K-major operands, 128B swizzle).
   auto issue_s = [&](int t, uint32_t kst) {
+    const uint32_t a0 = q_lo + t * kTile16;
+    const uint32_t b0 = k_lo + kst * kTile16;
+    const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-      const uint64_t a = sdesc_sw128(q_addr + t * C::kTileBytes + off, 16, 1024);
-      const uint64_t bdesc = sdesc_sw128(kv_addr + kst * C::kTileBytes + off, 16, 1024);
-      mma_ss(tmem + colS[t], a, bdesc, C::kIdescQK, kk > 0 ? 1u : 0u);
+      const uint32_t off = ((kk >> 2) * kSubBytes + (kk & 3) * 32) >> 4;
+      const uint64_t a = desc_from_words(a0 + off, kHi);
+      const uint64_t b = desc_from_words(b0 + off, kHi);
+      if (kk == 0)
+        mma_ss_c<0>(d, a, b, C::kIdescQK);
+      else
+        mma_ss_c<1>(d, a, b, C::kIdescQK);
     }
   };
-  // O_t (+)= P_t V over 128 keys in steps of 16 (P from TMEM, V MN-major).
-  auto issue_pv = [&](int t, uint32_t vst, bool accumulate) {
+  // O_t (+)= P_t V for key steps [kk0, kk0+4) (P from TMEM, V MN-major).
+  auto issue_pv_half = [&](int t, uint32_t vst, int half, bool first) {
+    const uint32_t b0 = v_lo + vst * kTile16;
+    const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+    const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t bdesc = sdesc_sw128(kv_addr + vst * C::kTileBytes + kk * 2048, kSubBytes, 1024);
-      mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, bdesc, C::kIdescPV,
-             (accumulate || kk > 0) ? 1u : 0u);
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int kk = half * 4 + k4;
+      const uint64_t bd = desc_from_words(b0 + kk * (2048 >> 4), kHi);
+      if (first && kk == 0)
+        mma_ts_c<0>(d, a + kk * 8, bd, C::kIdescPV);
+      else
+        mma_ts_c<1>(d, a + kk * 8, bd, C::kIdescPV);
     }
   };
   auto acquire_kv = [&](uint32_t& st) -> bool {
     st = kv_ctr % C::kStages;
     if (!wait_or_abort(&bars->kv_full[st], (kv_ctr / C::kStages) & 1, bars)) return false;
     ++kv_ctr;
-    tc_fence_after();
     return true;
   };
 
@@ -250,54 +275,53 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
     if (n == 0) continue;
     if (!(ok = wait_or_abort(&bars->q_full, q_ctr & 1, bars))) break;
     ++q_ctr;
-    tc_fence_after();
 
+    // Q may be overwritten once the item's last S MMA has completed.
+    int s_left = it.n[0] + it.n[1];
+    auto issue_s_counted = [&](int t, uint32_t st) {
+      issue_s(t, st);
+      tc_commit(&bars->s_full[t]);
+      if (--s_left == 0) tc_commit(&bars->q_empty);
+    };
     uint32_t kst;
     if (!(ok = acquire_kv(kst))) break;
+    tc_fence_after();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      if (it.n[t] > 0) {
-        issue_s(t, kst);
-        tc_commit(&bars->s_full[t]);
-      }
+      if (it.n[t] > 0) issue_s_counted(t, kst);
     }
     tc_commit(&bars->kv_empty[kst]);
 
     for (int j = 0; j < n && ok; ++j) {
-      uint32_t vst;
+      // Both operand tiles of this step are acquired before any P wait, so
+      // their (usually already satisfied) waits overlap queued MMAs.
+      uint32_t vst, nkst = 0;
+      const bool has_next = j + 1 < n;
       if (!(ok = acquire_kv(vst))) break;
-      uint32_t nkst = 0;
-      bool have_next = false;
+      if (has_next && !(ok = acquire_kv(nkst))) break;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= it.n[t]) continue;
-        if (!(ok = wait_or_abort(&bars->p_full[t], p_phase[t], bars))) break;
-        p_phase[t] ^= 1;
-        tc_fence_after();
-        issue_pv(t, vst, j > 0);
-        if (j == it.n[t] - 1) {
-          tc_commit(&bars->o_full[t]);
-        } else {
-          if (!have_next) {
-            if (!(ok = acquire_kv(nkst))) break;
-            have_next = true;
-          }
-          issue_s(t, nkst);
-          tc_commit(&bars->s_full[t]);
+        // P arrives in two halves (keys 0-63, 64-127): start on the first
+        // while the softmax warps are still producing the second.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          if (!(ok = wait_or_abort(&bars->p_full[t][half], p_phase[t], bars))) break;
+          tc_fence_after();
+          issue_pv_half(t, vst, half, j == 0);
         }
+        if (!ok) break;
+        p_phase[t] ^= 1;
+        if (j == it.n[t] - 1)
+          tc_commit(&bars->o_full[t]);
+        else
+          issue_s_counted(t, nkst);
       }
       if (!ok) break;
       tc_commit(&bars->kv_empty[vst]);
-      if (j + 1 < n) {
-        if (!have_next) {
-          if (!(ok = acquire_kv(nkst))) break;
-          have_next = true;
-        }
-        tc_commit(&bars->kv_empty[nkst]);
-      }
+      if (has_next) tc_commit(&bars->kv_empty[nkst]);
     }
     if (!ok) break;
-    tc_commit(&bars->q_empty);
   }
   if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
   // Every MMA this thread issued must finish before TMEM is released.
@@ -348,31 +372,37 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
       s_phase ^= 1;
       tc_fence_after();
 
-      uint32_t sr[128];
-      tmem_ld64(tS, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_ld64(tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
-      float* s = reinterpret_cast<float*>(sr);
-
+      // S row: columns 0..63 are loaded and waited for, 64..127 stay in
+      // flight while the first half is masked and reduced.
+      uint32_t sa[64], sb[64];
+      tmem_ld64(tS, sa);
+      tmem_ld64_nowait(tS + 64, sb);
       const int key0 = j * 128;
-      if (__any_sync(0xffffffffu, key0 + 127 > limit)) {
+      const bool need_mask = __any_sync(0xffffffffu, key0 + 127 > limit);
+      if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (key0 + c > limit) s[c] = -INFINITY;
+        for (int c = 0; c < 64; ++c)
+          if (key0 + c > limit) sa[c] = __float_as_uint(-INFINITY);
       }
-      // Row maximum with 8 independent chains (a single chain would serialise
-      // 127 dependent max operations).
-      float mx8[8];
+      // Row maximum: 4 independent chains of 3-input max.
+      float ch[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+      for (int c = 0; c < 64; c += 8)
 #pragma unroll
-      for (int c = 8; c < 128; c += 8)
+        for (int e = 0; e < 4; ++e)
+          ch[e] = max3(ch[e], __uint_as_float(sa[c + e]), __uint_as_float(sa[c + 4 + e]));
+      tmem_ld_wait64(sb);
+      if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
+        for (int c = 0; c < 64; ++c)
+          if (key0 + 64 + c > limit) sb[c] = __float_as_uint(-INFINITY);
+      }
 #pragma unroll
-      for (int w = 4; w > 0; w >>= 1)
+      for (int c = 0; c < 64; c += 8)
 #pragma unroll
-        for (int e = 0; e < w; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w]);
-      const float m_tile = mx8[0] * sl2;
+        for (int e = 0; e < 4; ++e)
+          ch[e] = max3(ch[e], __uint_as_float(sb[c + e]), __uint_as_float(sb[c + 4 + e]));
+      const float m_tile = max3(ch[0], ch[1], fmaxf(ch[2], ch[3])) * sl2;
 
       bool rescale = false;
       float alpha = 1.f;
@@ -386,34 +416,60 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O_t(j-1) is complete: S_t(j) was committed after O_t += P_t(j-1) V.
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t orow[32];
           tmem_ld32(tO + c, orow);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
+          for (int e = 0; e < 32; e += 2) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(orow[e]), __uint_as_float(orow[e + 1])), a2),
+                      x0, x1);
+            orow[e] = __float_as_uint(x0);
+            orow[e + 1] = __float_as_uint(x1);
+          }
           tmem_st32(tO + c, orow);
         }
       }
+      // p = 2^(s * scale * log2 e - m), two columns per paired FMA/ADD.
       const float base = (m == -INFINITY) ? 0.f : m;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t sc2 = f2_pack(sl2, sl2);
+      const uint64_t nb2 = f2_pack(-base, -base);
+      uint64_t acc2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc2[e] = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        const uint32_t* src = c < 2 ? &sa[32 * c] : &sb[32 * (c - 2)];
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(s[32 * c + 2 * e], sl2, -base));
-          const float p1 = ex2(fmaf(s[32 * c + 2 * e + 1], sl2, -base));
-          rs[e & 3] += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(src[2 * e]), __uint_as_float(src[2 * e + 1])),
+                           sc2, nb2),
+                    x0, x1);
+          const float p0 = ex2(x0);
+          const float p1 = ex2(x1);
+          acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + 16 * c, pk);
+        if (c & 1) {
+          // Keys [64*(c/2), 64*(c/2)+64) of P (and any O rescale) are in TMEM.
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[t][c >> 1]);
+        }
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
+      float rsum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a, b;
+        f2_unpack(acc2[e], a, b);
+        rsum += a + b;
+      }
+      l += rsum;
     }
     if (!ok) break;
 
@@ -465,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t][0], 128);
+      mbar_init(&bars->p_full[t][1], 128);
       mbar_init(&bars->o_full[t], 1);
     }
     mbar_init(&bars->mma_done, 1);
@@ -486,12 +543,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Register split: the softmax warpgroups hold a full S row; the MMA/TMA
+  // warpgroup needs few.  256*kRegsSoftmax + 128*kRegsOther equals the
+  // launch allocation of 384 threads x 168 registers (checked at build time).
   if (warp < 8) {
+    setmaxnreg_inc<kRegsSoftmax>();
     softmax_role<D>(p, bars, tmem, warp, lane);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role<D>(p, sQ, sKV, bars, tmem);
-  } else if (warp == kLoadWarp) {
-    if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+  } else {
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == kMmaWarp) {
+      if (lane == 0) mma_role<D>(p, sQ, sKV, bars, tmem);
+    } else if (warp == kLoadWarp) {
+      if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+    }
   }
 
   tc_fence_before();
