@@ -2,7 +2,9 @@
 // per-device state (SM count, kernel attributes, device status word).  Every
 // entry point validates before launching; nothing here allocates device
 // memory or synchronises, except attn_debug_status().
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
@@ -93,6 +95,39 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
   return cudaSuccess;
 }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, int D, int rows, int planes,
+                     int box_rows) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(rows), cuuint64_t(planes)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(D) * 2 * cuuint64_t(rows)};
+  const cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -147,7 +182,7 @@ int attn_decode_splitkv(const void* q, const void* k, const void* v, float* o_pa
   if (Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hkv * Sk * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
-  const int head_slices = (Hq / Hkv + 3) / 4;
+  const int head_slices = (Hq / Hkv + 15) / 16;  // query heads per decode CTA: 16
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535)
     return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;

@@ -3,24 +3,26 @@
 //
 // Source: "A Thread-Register Decoupled GPU Execution Model for Efficient Tensor
 // Computation", Methodology and Evaluation: decode attention (FlashDecoding) is
-// GEMV plus softmax, highly memory bound, and does not use the tensor cores.
-// The kernel therefore streams K and V once from HBM through shared memory with
-// bulk copies and does the arithmetic on the CUDA cores in fp32.
+// GEMV plus softmax and highly memory bound.  The kernel streams every K and V
+// byte exactly once from HBM with TMA and keeps the arithmetic far below the
+// memory time.
 //
-// decode kernel, one CTA per (split, KV head, batch) [x 4-head slice of the
-// query group when the group is wider than 4]:
-//   * the CTA's 4 query heads share every K/V byte it reads (GQA);
-//   * each of its 4 warps owns every 4th block of 32 keys of the split and
-//     keeps its own online-softmax state; each warp has a private ring of
-//     shared-memory slots filled by cp.async.bulk (K block, V block, K, V, ...),
-//     so warps never wait on each other while streaming;
-//   * inside a warp, lanes form 4 groups of 8; a group works on one key at a
-//     time, each lane holding D/8 dimensions: QK partial dot products are
-//     reduced across the 8 lanes with a reduce-scatter (3 shuffle rounds), so
-//     afterwards lane `sub` of group `grp` owns the scores of key 4*sub+grp;
-//   * P*V accumulates into per-lane registers (4 heads x D/8 dims); the warps'
-//     states are merged through shared memory at the end.
-// Scores are kept in the log2 domain: q is pre-multiplied by scale*log2(e).
+// decode kernel, one CTA per (split, KV head, batch) [x 16-head slice of the
+// query group when the group is wider than 16]:
+//   * the CTA's query heads (up to 16, the M rows of an m16n8k16 MMA) share
+//     every K/V byte it reads (GQA);
+//   * each of its 4 warps owns every 4th block of 32 keys of the split, keeps
+//     its own online-softmax state and has a private ring of shared-memory
+//     slots filled by 128-byte-swizzled TMA copies (K block, V block, ...), so
+//     warps never wait on each other while streaming;
+//   * S = Q K^T and O += P V run on mma.sync (bf16 in, fp32 accumulate) with
+//     ldmatrix / ldmatrix.trans fragments; the online softmax works directly on
+//     the accumulator fragments; P is rounded to bf16 for the second MMA;
+//   * the warps' states are merged through shared memory at the end.
+// Scores are kept in the log2 domain (scaled by scale * log2 e).  The running
+// maximum is moved lazily (only when it grows by more than 8) so the O
+// fragments are rarely rescaled; O and l always share one reference maximum.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,47 +37,75 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kHeads = 4;    // query heads per CTA
+constexpr int kRows = 16;    // query heads per CTA: the M rows of the MMA
 constexpr int kBlk = 32;     // keys per block
 constexpr int kWarps = 4;    // warps per CTA
 constexpr int kSlots = 3;    // ring slots per warp
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLazyRescale = 8.0f;
 
 template <int D>
-struct DecodeSmem {
-  alignas(128) uint8_t ring[kWarps][kSlots][kBlk * D * 2];
-  alignas(16) float p[kWarps][kBlk][kHeads];   // this block's softmax numerators
-  alignas(16) float red_o[kWarps][kHeads][D];  // per-warp partial outputs
-  float red_m[kWarps][kHeads];
-  float red_l[kWarps][kHeads];
-  alignas(8) uint64_t full[kWarps][kSlots];
+struct DecCfg {
+  static constexpr int kSub = D / 64;                       // 64-dim swizzled sub-tiles
+  static constexpr uint32_t kSubBytes = kBlk * 128;         // [32 keys x 64 dims] bf16
+  static constexpr uint32_t kSlotBytes = kSub * kSubBytes;  // one K or V block
+  static constexpr size_t kRingBytes = size_t(kWarps) * kSlots * kSlotBytes;
+  static constexpr size_t kStatBytes = 2 * kWarps * kRows * sizeof(float);
+  static constexpr size_t kSmemBytes =
+      1024 + kRingBytes + kStatBytes + kWarps * kSlots * sizeof(uint64_t);
+  // The per-warp partial outputs reuse the ring once streaming is over.
+  static_assert(size_t(kWarps) * kRows * D * sizeof(float) <= kRingBytes, "ring reuse");
 };
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
 
 __device__ __forceinline__ void record_status(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// c += a * b, m16n8k16, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared address of 16-byte chunk `cidx` (dims 8*cidx..8*cidx+7) of key row
+// `key` in a block stored as 64-dim sub-tiles with the TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int key, int cidx) {
+  return base + (cidx >> 3) * (kBlk * 128) + key * 128 + ((((cidx & 7) ^ (key & 7))) << 4);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32, 2)
-    decode_splitkv_kernel(const __nv_bfloat16* __restrict__ q,
-                          const __nv_bfloat16* __restrict__ k,
-                          const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
+    decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __nv_bfloat16* __restrict__ q, float* __restrict__ o_part,
                           float* __restrict__ lse_part, int B, int Hq, int Hkv, int Sk,
-                          int chunk, int head_slices, float qscale, int* status) {
-  constexpr int NCH = D / 64;           // 16-byte chunks per lane per row
-  constexpr int DL = 8 * NCH;           // dimensions per lane
-  constexpr uint32_t kRowBytes = D * 2;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  DecodeSmem<D>& sm = *reinterpret_cast<DecodeSmem<D>*>(smem_raw);
+                          int chunk, int head_slices, float scale_log2, int* status) {
+  using C = DecCfg<D>;
+  constexpr int KS = D / 16;  // k-steps of S = Q K^T
+  constexpr int NT = D / 8;   // n-tiles of O += P V
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  float* red_m = reinterpret_cast<float*>(smem + C::kRingBytes);  // [warp][row]
+  float* red_l = red_m + kWarps * kRows;                           // [warp][row]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red_l + kWarps * kRows);  // [warp][slot]
+  float* red_o = reinterpret_cast<float*>(ring);                   // [warp][row][D], after streaming
 
   const int split = blockIdx.x;
   const int g = blockIdx.y / head_slices;
@@ -84,8 +114,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   const int G = Hq / Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int grp = lane >> 3;
-  const int sub = lane & 7;
+  const int grp = lane >> 2;  // MMA group: rows grp and grp + 8
+  const int tq = lane & 3;    // thread in group
 
   const long long kb64 = static_cast<long long>(split) * chunk;
   const int key_begin = kb64 < Sk ? static_cast<int>(kb64) : Sk;
@@ -94,141 +124,84 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   const int nblk = (nkeys + kBlk - 1) / kBlk;
   const int my_nblk = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
   const int nloads = 2 * my_nblk;
+  const int bkv = b * Hkv + g;
 
-  const size_t kv_off = (static_cast<size_t>(b) * Hkv + g) * static_cast<size_t>(Sk) * D;
-  const __nv_bfloat16* kbase = k + kv_off;
-  const __nv_bfloat16* vbase = v + kv_off;
-
+  uint64_t* my_full = full + warp * kSlots;
+  uint8_t* my_ring = ring + size_t(warp) * kSlots * C::kSlotBytes;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) mbar_init(&sm.full[warp][s], 1);
+    for (int s = 0; s < kSlots; ++s) mbar_init(&my_full[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
 
-  const uint64_t policy = policy_evict_first();
   // Load number li of this warp: even = K block, odd = V block of its (li/2)-th block.
   auto issue = [&](int li) {
-    const int blk = warp + (li >> 1) * kWarps;
-    const int key0 = key_begin + blk * kBlk;
-    const int rows = min(kBlk, key_end - key0);
-    const __nv_bfloat16* src = ((li & 1) ? vbase : kbase) + static_cast<size_t>(key0) * D;
+    const int key0 = key_begin + (warp + (li >> 1) * kWarps) * kBlk;
     const int slot = li % kSlots;
-    const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
-    mbar_arrive_expect_tx(&sm.full[warp][slot], bytes);
-    bulk_load(sm.ring[warp][slot], src, bytes, &sm.full[warp][slot], policy);
+    uint8_t* dst = my_ring + slot * C::kSlotBytes;
+    mbar_arrive_expect_tx(&my_full[slot], C::kSlotBytes);
+#pragma unroll
+    for (int s = 0; s < C::kSub; ++s)
+      tma_load_3d(dst + s * C::kSubBytes, (li & 1) ? &tmV : &tmK, &my_full[slot], s * 64, key0,
+                  bkv);
   };
   int issued = 0;
   if (lane == 0) {
     for (; issued < kSlots && issued < nloads; ++issued) issue(issued);
   }
 
-  // This CTA's query heads: slice*4 + t of the group, t < 4.
-  float qf[kHeads][DL];
+  // Q as the A operand: rows grp (regs 0, 2) and grp + 8 (regs 1, 3).
+  uint32_t qa[KS][4];
+  {
+    const int h0 = slice * kRows + grp, h1 = h0 + 8;
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+        q + (static_cast<size_t>(b) * Hq + g * G + min(h0, G - 1)) * D);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+        q + (static_cast<size_t>(b) * Hq + g * G + min(h1, G - 1)) * D);
+    const bool v0 = h0 < G, v1 = h1 < G;
 #pragma unroll
-  for (int t = 0; t < kHeads; ++t) {
-    const int hl = slice * kHeads + t;
-    if (hl < G) {
-      const int hq = g * G + hl;
-      const uint4* qrow =
-          reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq) * D);
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float f[8];
-        bf16x8_to_f32(__ldg(qrow + c * 8 + sub), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qf[t][c * 8 + e] = f[e] * qscale;
-      }
-    } else {
-#pragma unroll
-      for (int d = 0; d < DL; ++d) qf[t][d] = 0.f;
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = v0 ? __ldg(q0 + 8 * ks + tq) : 0u;
+      qa[ks][1] = v1 ? __ldg(q1 + 8 * ks + tq) : 0u;
+      qa[ks][2] = v0 ? __ldg(q0 + 8 * ks + 4 + tq) : 0u;
+      qa[ks][3] = v1 ? __ldg(q1 + 8 * ks + 4 + tq) : 0u;
     }
   }
 
-  float m_run[kHeads], l_lane[kHeads], acc[kHeads][DL];
+  float o[NT][4];
 #pragma unroll
-  for (int t = 0; t < kHeads; ++t) {
-    m_run[t] = -INFINITY;
-    l_lane[t] = 0.f;
-#pragma unroll
-    for (int d = 0; d < DL; ++d) acc[t][d] = 0.f;
-  }
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};  // rows grp, grp + 8 (log2 domain)
+  float l_run[2] = {0.f, 0.f};              // this lane's part of the row sums
 
   bool ok = true;
   int consumed = 0;
   for (int i = 0; i < my_nblk && ok; ++i) {
-    const int blk = warp + i * kWarps;
-    const int key0 = key_begin + blk * kBlk;
+    const int key0 = key_begin + (warp + i * kWarps) * kBlk;
     const int nvalid = min(kBlk, key_end - key0);
 
-    // ---------------- K block: scores for 32 keys x 4 heads
+    // ---------------- K block: S = Q K^T for 32 keys (4 n-tiles of 8 keys)
+    float s[4][4];
     {
       const int li = 2 * i;
       const int slot = li % kSlots;
-      ok = mbar_wait(&sm.full[warp][slot], (li / kSlots) & 1);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, mbar_wait(&my_full[slot], (li / kSlots) & 1));
       if (!ok) break;
       consumed = li + 1;
-      const uint8_t* kb = sm.ring[warp][slot];
-      float part[32];  // index 4*t + head, key 4*t + grp
+      const uint32_t kb = smem_u32(my_ring + slot * C::kSlotBytes);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const uint4* row = reinterpret_cast<const uint4*>(kb + (4 * t + grp) * kRowBytes);
-        float kf[DL];
+      for (int nt = 0; nt < 4; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        const int key = 8 * nt + (lane & 7);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) bf16x8_to_f32(row[c * 8 + sub], kf + c * 8);
-#pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          float s = 0.f;
-#pragma unroll
-          for (int d = 0; d < DL; ++d) s = fmaf(qf[h][d], kf[d], s);
-          part[4 * t + h] = s;
+        for (int kp = 0; kp < KS / 2; ++kp) {
+          uint32_t r[4];
+          ldsm_x4(swz(kb, key, 4 * kp + (lane >> 3)), r);
+          mma_16816(s[nt], qa[2 * kp], r[0], r[1]);
+          mma_16816(s[nt], qa[2 * kp + 1], r[2], r[3]);
         }
       }
-      // Reduce-scatter across the 8 lanes of the group.
-#pragma unroll
-      for (int i2 = 0; i2 < 16; ++i2) {
-        const bool up = lane & 4;
-        const float send = up ? part[i2] : part[i2 + 16];
-        const float keep = up ? part[i2 + 16] : part[i2];
-        part[i2] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-      }
-#pragma unroll
-      for (int i2 = 0; i2 < 8; ++i2) {
-        const bool up = lane & 2;
-        const float send = up ? part[i2] : part[i2 + 8];
-        const float keep = up ? part[i2 + 8] : part[i2];
-        part[i2] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-      }
-#pragma unroll
-      for (int i2 = 0; i2 < 4; ++i2) {
-        const bool up = lane & 1;
-        const float send = up ? part[i2] : part[i2 + 4];
-        const float keep = up ? part[i2 + 4] : part[i2];
-        part[i2] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-      }
-      const int jj = 4 * sub + grp;  // the key whose scores this lane now owns
-      const bool valid = jj < nvalid;
-      float pv[kHeads];
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h) {
-        const float sc = valid ? part[h] : -INFINITY;
-        float mb = sc;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
-        const float mn = fmaxf(m_run[h], mb);
-        const float base = (mn == -INFINITY) ? 0.f : mn;
-        const float alpha = ex2(m_run[h] - base);
-        pv[h] = ex2(sc - base);
-        m_run[h] = mn;
-        l_lane[h] = fmaf(l_lane[h], alpha, pv[h]);
-        if (alpha != 1.f) {  // warp-uniform: m_run and base are uniform
-#pragma unroll
-          for (int d = 0; d < DL; ++d) acc[h][d] *= alpha;
-        }
-      }
-      *reinterpret_cast<float4*>(&sm.p[warp][jj][0]) = make_float4(pv[0], pv[1], pv[2], pv[3]);
       __syncwarp();
       if (lane == 0 && li + kSlots < nloads) {
         fence_proxy_async_smem();
@@ -237,29 +210,77 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       }
     }
 
-    // ---------------- V block: acc += p * V
+    // ---------------- online softmax on the S fragments
+    uint32_t pa[2][4];  // P as the A operand of the two 16-key steps
+    {
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = 8 * nt + 2 * tq + (e & 1);
+          const float x = key < nvalid ? s[nt][e] * scale_log2 : -INFINITY;
+          s[nt][e] = x;
+          mx[e >> 1] = fmaxf(mx[e >> 1], x);
+        }
+      float alpha[2];
+      bool need = false;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        alpha[r] = 1.f;
+        if (m_run[r] == -INFINITY || mx[r] > m_run[r] + kLazyRescale) {
+          alpha[r] = ex2(m_run[r] - mx[r]);  // 0 on the first block
+          m_run[r] = mx[r];
+          l_run[r] *= alpha[r];
+          need = true;
+        }
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[nt][0] *= alpha[0];
+          o[nt][1] *= alpha[0];
+          o[nt][2] *= alpha[1];
+          o[nt][3] *= alpha[1];
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pv = ex2(s[nt][e] - m_run[e >> 1]);
+          s[nt][e] = pv;
+          l_run[e >> 1] += pv;
+        }
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        pa[kk][0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+        pa[kk][1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+        pa[kk][2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        pa[kk][3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      }
+    }
+
+    // ---------------- V block: O += P V (two 16-key steps x D/8 n-tiles)
     {
       const int li = 2 * i + 1;
       const int slot = li % kSlots;
-      ok = mbar_wait(&sm.full[warp][slot], (li / kSlots) & 1);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, mbar_wait(&my_full[slot], (li / kSlots) & 1));
       if (!ok) break;
       consumed = li + 1;
-      const uint8_t* vb = sm.ring[warp][slot];
+      const uint32_t vb = smem_u32(my_ring + slot * C::kSlotBytes);
+      const int mat = lane >> 3;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int j = 4 * t + grp;
-        if (j < nvalid) {
-          const float4 pp = *reinterpret_cast<const float4*>(&sm.p[warp][j][0]);
-          const float ph[4] = {pp.x, pp.y, pp.z, pp.w};
-          const uint4* row = reinterpret_cast<const uint4*>(vb + j * kRowBytes);
-          float vf[DL];
+      for (int kk = 0; kk < 2; ++kk) {
+        const int key = 16 * kk + (mat & 1) * 8 + (lane & 7);
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) bf16x8_to_f32(row[c * 8 + sub], vf + c * 8);
-#pragma unroll
-          for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-            for (int d = 0; d < DL; ++d) acc[h][d] = fmaf(ph[h], vf[d], acc[h][d]);
+        for (int ndp = 0; ndp < NT / 2; ++ndp) {
+          uint32_t r[4];
+          ldsm_x4_t(swz(vb, key, 2 * ndp + (mat >> 1)), r);
+          mma_16816(o[2 * ndp], pa[kk], r[0], r[1]);
+          mma_16816(o[2 * ndp + 1], pa[kk], r[2], r[3]);
         }
       }
       __syncwarp();
@@ -277,87 +298,73 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     record_status(status, ATTN_ERR_TIMEOUT);
     if (lane == 0) {
       for (int li = consumed; li < issued; ++li)
-        (void)mbar_wait(&sm.full[warp][li % kSlots], (li / kSlots) & 1);
+        (void)mbar_wait(&my_full[li % kSlots], (li / kSlots) & 1);
     }
     __syncwarp();
   }
 
-  // ---------------- merge: lanes of a warp, then the warps of the CTA
+  // ---------------- merge: the 4 lanes of a row, then the warps of the CTA
 #pragma unroll
-  for (int h = 0; h < kHeads; ++h) {
-    float l = l_lane[h];
+  for (int r = 0; r < 2; ++r) {
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+  }
+  __syncthreads();  // every warp is done with the ring: reuse it for red_o
+  {
+    float* mine = red_o + size_t(warp) * kRows * D;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    l_lane[h] = l;
-#pragma unroll
-    for (int d = 0; d < DL; ++d) {
-      float a = acc[h][d];
-      a += __shfl_xor_sync(0xffffffffu, a, 8);
-      a += __shfl_xor_sync(0xffffffffu, a, 16);
-      acc[h][d] = a;
+    for (int nt = 0; nt < NT; ++nt) {
+      *reinterpret_cast<float2*>(mine + grp * D + 8 * nt + 2 * tq) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(mine + (grp + 8) * D + 8 * nt + 2 * tq) =
+          make_float2(o[nt][2], o[nt][3]);
     }
-  }
-  if (grp == 0) {
-#pragma unroll
-    for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float4* dst = reinterpret_cast<float4*>(&sm.red_o[warp][h][c * 64 + sub * 8]);
-        dst[0] = make_float4(acc[h][c * 8 + 0], acc[h][c * 8 + 1], acc[h][c * 8 + 2],
-                             acc[h][c * 8 + 3]);
-        dst[1] = make_float4(acc[h][c * 8 + 4], acc[h][c * 8 + 5], acc[h][c * 8 + 6],
-                             acc[h][c * 8 + 7]);
-      }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < kHeads; ++h) {
-      sm.red_m[warp][h] = m_run[h];
-      sm.red_l[warp][h] = l_lane[h];
+    if (tq == 0) {
+      red_m[warp * kRows + grp] = m_run[0];
+      red_m[warp * kRows + grp + 8] = m_run[1];
+      red_l[warp * kRows + grp] = l_run[0];
+      red_l[warp * kRows + grp + 8] = l_run[1];
     }
   }
   __syncthreads();
 
-  // Thread layout for the final merge: head h = warp, D/32 dims per lane.
+  // 128 threads: row r = tid / 8 (16 rows), D/8 dims each.
   {
-    const int h = warp;
-    const int hl = slice * kHeads + h;
+    const int r = threadIdx.x >> 3;
+    const int part = threadIdx.x & 7;
+    const int hl = slice * kRows + r;
     if (hl < G) {
       const int hq = g * G + hl;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.red_m[w][h]);
-      constexpr int DPL = D / 32;
-      float out[DPL];
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * kRows + r]);
+      constexpr int DPT = D / 8;
+      float out[DPT];
+#pragma unroll
+      for (int e = 0; e < DPT; ++e) out[e] = 0.f;
       float lse;
       if (M == -INFINITY) {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) out[e] = 0.f;
         lse = -INFINITY;
       } else {
         float L = 0.f;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) out[e] = 0.f;
-#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-          const float wt = ex2(sm.red_m[w][h] - M);
-          L = fmaf(wt, sm.red_l[w][h], L);
+          const float wt = ex2(red_m[w * kRows + r] - M);
+          L = fmaf(wt, red_l[w * kRows + r], L);
+          const float* src = red_o + (size_t(w) * kRows + r) * D + part * DPT;
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) out[e] = fmaf(wt, sm.red_o[w][h][lane * DPL + e], out[e]);
+          for (int e = 0; e < DPT; ++e) out[e] = fmaf(wt, src[e], out[e]);
         }
         const float inv = 1.f / L;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) out[e] *= inv;
+        for (int e = 0; e < DPT; ++e) out[e] *= inv;
         lse = (M + log2f(L)) * kLn2;
       }
       const size_t row = (static_cast<size_t>(split) * B + b) * Hq + hq;
-      float* dst = o_part + row * D + lane * DPL;
-      if constexpr (DPL == 4) {
-        *reinterpret_cast<float4*>(dst) = make_float4(out[0], out[1], out[2], out[3]);
-      } else {
-        *reinterpret_cast<float2*>(dst) = make_float2(out[0], out[1]);
-      }
-      if (lane == 0) lse_part[row] = lse;
+      float* dst = o_part + row * D + part * DPT;
+#pragma unroll
+      for (int e = 0; e < DPT; e += 4)
+        *reinterpret_cast<float4*>(dst + e) = make_float4(out[e], out[e + 1], out[e + 2], out[e + 3]);
+      if (part == 0) lse_part[row] = lse;
     }
   }
 }
@@ -420,19 +427,22 @@ template <int D>
 cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, float* o_part,
                                float* lse_part, int B, int Hq, int Hkv, int Sk, int num_splits,
                                float scale, cudaStream_t stream, int* status) {
+  using C = DecCfg<D>;
   const int G = Hq / Hkv;
-  const int head_slices = (G + kHeads - 1) / kHeads;
+  const int head_slices = (G + kRows - 1) / kRows;
   const int chunk = (Sk + num_splits - 1) / num_splits;
-  const size_t smem = sizeof(DecodeSmem<D>);
+  CUtensorMap tmK, tmV;
+  if (!encode_bf16_map(&tmK, k, D, Sk, B * Hkv, kBlk) ||
+      !encode_bf16_map(&tmV, v, D, Sk, B * Hkv, kBlk))
+    return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(decode_splitkv_kernel<D>),
-                                   static_cast<int>(smem));
+                                   static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const dim3 grid(num_splits, Hkv * head_slices, B);
-  const float qscale = scale * 1.4426950408889634f;
-  decode_splitkv_kernel<D><<<grid, kWarps * 32, smem, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), o_part, lse_part, B, Hq, Hkv, Sk, chunk,
-      head_slices, qscale, status);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  decode_splitkv_kernel<D><<<grid, kWarps * 32, C::kSmemBytes, stream>>>(
+      tmK, tmV, static_cast<const __nv_bfloat16*>(q), o_part, lse_part, B, Hq, Hkv, Sk, chunk,
+      head_slices, scale_log2, status);
   return cudaGetLastError();
 }
 
@@ -513,7 +523,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* k, const void* v, 
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hkv * Sk * D > (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
-  const int head_slices = (Hq / Hkv + 3) / 4;
+  const int head_slices = (Hq / Hkv + 15) / 16;
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535) return ATTN_ERR_UNSUPPORTED;
   // The partials must fit the static scratch array.
   const long long part_floats = static_cast<long long>(num_splits) * B * Hq * D;

@@ -37,7 +37,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <cstdint>
@@ -568,42 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult qres;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &qres) == cudaSuccess &&
-        qres == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// [planes, rows, D] bf16 tensor, boxes of [1, 128, 64] with 128-byte swizzle.
-bool encode_map(CUtensorMap* map, const void* base, int D, int rows, int planes) {
-  auto fn = get_encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(rows), cuuint64_t(planes)};
-  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(D) * 2 * cuuint64_t(rows)};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, float* o, float* lse,
                             int B, int Hq, int Hkv, int Sq, int Sk, int causal, float scale,
                             cudaStream_t stream, int* status) {
   using C = Cfg<D>;
   CUtensorMap tmQ, tmK, tmV;
-  if (!encode_map(&tmQ, q, D, Sq, B * Hq) || !encode_map(&tmK, k, D, Sk, B * Hkv) ||
-      !encode_map(&tmV, v, D, Sk, B * Hkv))
+  if (!encode_bf16_map(&tmQ, q, D, Sq, B * Hq, 128) || !encode_bf16_map(&tmK, k, D, Sk, B * Hkv, 128) ||
+      !encode_bf16_map(&tmV, v, D, Sk, B * Hkv, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(attn_fwd_kernel<D>),
                                    static_cast<int>(C::kSmemBytes));

@@ -1,6 +1,7 @@
 // internal.h -- declarations shared by the library's translation units (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -18,6 +19,12 @@ int sm_count();
 // Raise the kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device).
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+// Tiled TMA map of a contiguous [planes, rows, D] bf16 tensor with boxes of
+// [1, box_rows, 64] elements and 128-byte swizzle (rows past `rows` read as
+// zero).  False if the driver entry point is unavailable or rejects the map.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int D, int rows, int planes,
+                     int box_rows);
 
 // Kernel launchers; arguments are already validated.  Return cudaError_t of
 // the launch.

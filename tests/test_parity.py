@@ -183,10 +183,14 @@ def test_combine_alone_against_oracle():
 
 
 def test_decode_split_invariance_on_gpu():
+    # P is rounded to bf16 before P*V relative to each split's own reference
+    # maximum, so different splittings round differently: |dO| <= 2^-9 * max|V|
+    # bounds the difference; the LSE sums stay in fp32.
     q, k, v = make_qkv(2, 8, 2, 1, 777, 128, seed=42)
     outs = [gpu_decode(q, k, v, ns, 0.1)[2:] for ns in (1, 2, 3, 8, 16)]
+    vmax = float(v.float().abs().max())
     for o, lse in outs[1:]:
-        assert np.max(np.abs(o - outs[0][0])) <= 1e-4
+        assert np.max(np.abs(o - outs[0][0])) <= 2.0 ** -9 * vmax
         assert np.max(np.abs(lse - outs[0][1])) <= 1e-4
 
 
