@@ -370,6 +370,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 }
 
 // One warp per output row: lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+// Splits are handled 32 at a time: lane s holds split s's LSE and weight, the
+// max and sum are warp reductions, and the O loads of all splits of a chunk are
+// independent (lane-parallel over D, unrolled over splits).
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o_part,
                                                       const float* __restrict__ lse_part,
@@ -382,33 +385,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   float M = -INFINITY;
-  for (int s = 0; s < num_splits; ++s)
+  for (int s = lane; s < num_splits; s += 32)
     M = fmaxf(M, __ldg(lse_part + static_cast<size_t>(s) * rows + row));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float out[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) out[e] = 0.f;
-  float L;
-  if (M == -INFINITY) {
-    L = -INFINITY;
-  } else {
+  float L = -INFINITY;
+  if (M != -INFINITY) {
     float W = 0.f;
-    for (int s = 0; s < num_splits; ++s) {
-      const size_t r = static_cast<size_t>(s) * rows + row;
-      const float w = ex2((__ldg(lse_part + r) - M) * kLog2e);
-      W += w;
-      const float* src = o_part + r * D + lane * DPL;
-      if constexpr (DPL == 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(src));
-        out[0] = fmaf(w, x.x, out[0]);
-        out[1] = fmaf(w, x.y, out[1]);
-        out[2] = fmaf(w, x.z, out[2]);
-        out[3] = fmaf(w, x.w, out[3]);
-      } else {
-        const float2 x = __ldg(reinterpret_cast<const float2*>(src));
-        out[0] = fmaf(w, x.x, out[0]);
-        out[1] = fmaf(w, x.y, out[1]);
+    for (int c0 = 0; c0 < num_splits; c0 += 32) {
+      const int s_lane = c0 + lane;
+      const float w_lane =
+          s_lane < num_splits
+              ? ex2((__ldg(lse_part + static_cast<size_t>(s_lane) * rows + row) - M) * kLog2e)
+              : 0.f;
+      W += w_lane;
+      const int cnt = min(32, num_splits - c0);
+#pragma unroll 8
+      for (int k = 0; k < cnt; ++k) {
+        const float w = __shfl_sync(0xffffffffu, w_lane, k);
+        const float* src = o_part + (static_cast<size_t>(c0 + k) * rows + row) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+          out[0] = fmaf(w, x.x, out[0]);
+          out[1] = fmaf(w, x.y, out[1]);
+          out[2] = fmaf(w, x.z, out[2]);
+          out[3] = fmaf(w, x.w, out[3]);
+        } else {
+          const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+          out[0] = fmaf(w, x.x, out[0]);
+          out[1] = fmaf(w, x.y, out[1]);
+        }
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
     const float inv = 1.f / W;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) out[e] *= inv;
