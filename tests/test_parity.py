@@ -80,6 +80,17 @@ def test_head_grouping(Hq, Hkv):
     run_fwd_case(2, Hq, Hkv, 256, 384, 64, True, seed=Hq * 10 + Hkv)
 
 
+@pytest.mark.parametrize("Hq,Hkv,causal,S", [
+    (4, 4, True, 700),     # causal MHA, D=128: single-CTA kernel
+    (6, 2, True, 300),     # causal, group of 3: single-CTA kernel
+    (6, 2, False, 777),    # non-causal, group of 3: CTA pairs over row blocks
+    (3, 1, False, 1100),   # odd head count, row-block pairs, odd number of blocks
+    (8, 2, True, 1500),    # group of 4: CTA pairs over heads
+])
+def test_d128_kernel_forms(Hq, Hkv, causal, S):
+    run_fwd_case(2, Hq, Hkv, S, S, 128, causal, seed=Hq * 31 + S)
+
+
 def test_multi_item_per_cta():
     # More 256-row work items than SMs, so CTAs walk several items each.
     run_fwd_case(2, 48, 8, 1024, 1024, 64, True, seed=77)
