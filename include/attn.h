@@ -88,6 +88,29 @@ ATTN_API int attn_decode_splitkv(const void *q, const void *k, const void *v, fl
                         int num_splits, float scale, void *stream);
 
 /*
+ * Split-KV decode over sequences of different lengths (first stage).
+ * Source: "VDCores: Resource Decoupled Programming and Execution for
+ * Asynchronous GPUs", Evaluation (the dynamic-attention-length case study:
+ * decode requests whose KV lengths differ) applied to the FlashDecoding split
+ * of "A Thread-Register Decoupled GPU Execution Model for Efficient Tensor
+ * Computation", Methodology.
+ *
+ * Same as attn_decode_splitkv, except that sequence b attends only to its
+ * first seqlens[b] keys: k and v are [B,Hkv,Sk,D] buffers of capacity Sk per
+ * sequence, and keys at or past seqlens[b] are never read into the result
+ * (their contents may be anything, including NaN).  Each sequence is split on
+ * its own: chunk_b = ceil(seqlens[b] / num_splits).  A sequence of length 0
+ * yields O = 0 and LSE = -inf after attn_combine.
+ *
+ *   seqlens: device int32 [B], 4-byte aligned; values are clamped to [0, Sk].
+ *   Other arguments, layouts and errors as for attn_decode_splitkv.
+ */
+ATTN_API int attn_decode_splitkv_varlen(const void *q, const void *k, const void *v,
+                                        const int *seqlens, float *o_part, float *lse_part,
+                                        int B, int Hq, int Hkv, int Sk, int D, int num_splits,
+                                        float scale, void *stream);
+
+/*
  * Split-KV decode, second stage: log-sum-exp combine of the partials.
  * Source: same page (FlashDecoding's reduction across key splits).
  *   lse = ln sum_s exp(lse_s);  o = sum_s exp(lse_s - lse) * o_s

@@ -10,6 +10,7 @@ exception is raised.
 Names follow the C ABI:
     attn_fwd(q, k, v, causal, scale)            -> (o, lse)
     attn_decode_splitkv(q, k, v, num_splits)    -> (o_part, lse_part)
+    attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits) -> (o_part, lse_part)
     attn_combine(o_part, lse_part)              -> (o, lse)
     decode(q, k, v, num_splits)                 -> (o, lse)   both stages
 Layouts: Q [B,Hq,Sq,D], K/V [B,Hkv,Sk,D] bf16; O [B,Hq,Sq,D], LSE [B,Hq,Sq] fp32.
@@ -23,7 +24,8 @@ import threading
 
 import torch
 
-__all__ = ["AttnError", "attn_fwd", "attn_decode_splitkv", "attn_combine", "decode",
+__all__ = ["AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
+           "attn_combine", "decode",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
            "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
@@ -50,6 +52,8 @@ _SIGNATURES = {
                   _vp], _int),
     "attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                              _flt, _vp], _int),
+    "attn_decode_splitkv_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
+                                    _int, _flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
     "attn_debug_status": ([_vp], _int),
@@ -187,6 +191,41 @@ def attn_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_s
     return o_part, lse_part
 
 
+def attn_decode_splitkv_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               seqlens: torch.Tensor, num_splits: int,
+                               scale: float | None = None, o_part: torch.Tensor | None = None,
+                               lse_part: torch.Tensor | None = None, stream=None):
+    """Split-KV decode partials where sequence b attends to its first seqlens[b] keys.
+
+    k/v are [B,Hkv,Sk,D] buffers of capacity Sk; seqlens is an int32 CUDA tensor [B].
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    _check(Sq == 1, "decode takes one query row per head (q.shape[2] == 1)")
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(isinstance(seqlens, torch.Tensor) and seqlens.is_cuda and seqlens.dtype == torch.int32
+           and seqlens.is_contiguous() and tuple(seqlens.shape) == (B,),
+           "seqlens must be a contiguous int32 CUDA tensor of shape [B]")
+    _check(k.device == q.device and v.device == q.device and seqlens.device == q.device,
+           "q/k/v/seqlens must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ns = int(num_splits)
+    o_part = _out(o_part, (ns, B, Hq, D), q.device, "o_part")
+    lse_part = _out(lse_part, (ns, B, Hq), q.device, "lse_part")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_decode_splitkv_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            seqlens.data_ptr(), o_part.data_ptr(),
+                                            lse_part.data_ptr(), B, Hq, Hkv, Sk, D, ns,
+                                            float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_decode_splitkv_varlen")
+    return o_part, lse_part
+
+
 def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor | None = None,
                  lse: torch.Tensor | None = None, stream=None):
     """LSE combine: o_part [ns,B,Hq,D], lse_part [ns,B,Hq] -> (o [B,Hq,D], lse [B,Hq])."""
@@ -206,8 +245,17 @@ def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor |
 
 
 def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
-           scale: float | None = None, workspace=None, o=None, lse=None, stream=None):
-    """Split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq])."""
+           scale: float | None = None, workspace=None, o=None, lse=None, stream=None,
+           seqlens: torch.Tensor | None = None):
+    """Split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq]).
+
+    With ``seqlens`` (int32 CUDA [B]) sequence b attends to its first seqlens[b] keys.
+    """
     o_part, lse_part = (None, None) if workspace is None else workspace
-    o_part, lse_part = attn_decode_splitkv(q, k, v, num_splits, scale, o_part, lse_part, stream)
+    if seqlens is None:
+        o_part, lse_part = attn_decode_splitkv(q, k, v, num_splits, scale, o_part, lse_part,
+                                               stream)
+    else:
+        o_part, lse_part = attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits, scale,
+                                                      o_part, lse_part, stream)
     return attn_combine(o_part, lse_part, o, lse, stream)

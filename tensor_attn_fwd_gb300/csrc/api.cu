@@ -171,9 +171,11 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
-                        float* lse_part, int B, int Hq, int Hkv, int Sk, int D, int num_splits,
-                        float scale, void* stream) {
+namespace {
+
+int decode_common(const void* q, const void* k, const void* v, const int* seqlens,
+                  float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
+                  int num_splits, float scale, void* stream) {
   if (!q || !k || !v || !o_part || !lse_part) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -193,8 +195,26 @@ int attn_decode_splitkv(const void* q, const void* k, const void* v, float* o_pa
   if (status == nullptr) return ATTN_ERR_CUDA;
   const cudaError_t e =
       launch_decode_splitkv(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
-                            static_cast<cudaStream_t>(stream), status);
+                            static_cast<cudaStream_t>(stream), status, seqlens);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int attn_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
+                        float* lse_part, int B, int Hq, int Hkv, int Sk, int D, int num_splits,
+                        float scale, void* stream) {
+  return decode_common(q, k, v, nullptr, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
+                       stream);
+}
+
+int attn_decode_splitkv_varlen(const void* q, const void* k, const void* v, const int* seqlens,
+                               float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk,
+                               int D, int num_splits, float scale, void* stream) {
+  if (!seqlens) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  return decode_common(q, k, v, seqlens, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
+                       stream);
 }
 
 int attn_combine(const float* o_part, const float* lse_part, float* o, float* lse, int B, int Hq,

@@ -93,8 +93,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const __nv_bfloat16* __restrict__ q, float* __restrict__ o_part,
-                          float* __restrict__ lse_part, int B, int Hq, int Hkv, int Sk,
-                          int chunk, int head_slices, float scale_log2, int* status) {
+                          float* __restrict__ lse_part, const int* __restrict__ seqlens, int B,
+                          int Hq, int Hkv, int Sk, int num_splits, int head_slices,
+                          float scale_log2, int* status) {
   using C = DecCfg<D>;
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NT = D / 8;   // n-tiles of O += P V
@@ -117,9 +118,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   const int grp = lane >> 2;  // MMA group: rows grp and grp + 8
   const int tq = lane & 3;    // thread in group
 
+  // This sequence's keys: all Sk, or its own length (clamped to [0, Sk]).
+  const int len = seqlens != nullptr ? min(max(__ldg(seqlens + b), 0), Sk) : Sk;
+  const int chunk = (len + num_splits - 1) / num_splits;
   const long long kb64 = static_cast<long long>(split) * chunk;
-  const int key_begin = kb64 < Sk ? static_cast<int>(kb64) : Sk;
-  const int key_end = min(key_begin + chunk, Sk);
+  const int key_begin = kb64 < len ? static_cast<int>(kb64) : len;
+  const int key_end = min(key_begin + chunk, len);
   const int nkeys = key_end - key_begin;
   const int nblk = (nkeys + kBlk - 1) / kBlk;
   const int my_nblk = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
@@ -271,6 +275,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       if (!ok) break;
       consumed = li + 1;
       const uint32_t vb = smem_u32(my_ring + slot * C::kSlotBytes);
+      if (nvalid < kBlk) {
+        // Rows past the block's last key are real keys of another split, zero
+        // fill past Sk, or (with per-sequence lengths) unwritten cache memory
+        // that may hold NaN/Inf: zero them so that p = 0 contributes nothing.
+        uint8_t* vrow = my_ring + slot * C::kSlotBytes;
+        for (int idx = lane; idx < (kBlk - nvalid) * 8 * C::kSub; idx += 32) {
+          const int r = nvalid + idx / (8 * C::kSub);
+          const int c = idx % (8 * C::kSub);  // 16-byte chunk across the sub-tiles
+          *reinterpret_cast<uint4*>(vrow + (c >> 3) * C::kSubBytes + r * 128 + (c & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
       const int mat = lane >> 3;
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
@@ -437,13 +454,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 template <int D>
-cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, float* o_part,
-                               float* lse_part, int B, int Hq, int Hkv, int Sk, int num_splits,
-                               float scale, cudaStream_t stream, int* status) {
+cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, const int* seqlens,
+                               float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk,
+                               int num_splits, float scale, cudaStream_t stream, int* status) {
   using C = DecCfg<D>;
   const int G = Hq / Hkv;
   const int head_slices = (G + kRows - 1) / kRows;
-  const int chunk = (Sk + num_splits - 1) / num_splits;
   CUtensorMap tmK, tmV;
   if (!encode_bf16_map(&tmK, k, D, Sk, B * Hkv, kBlk) ||
       !encode_bf16_map(&tmV, v, D, Sk, B * Hkv, kBlk))
@@ -454,8 +470,8 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, floa
   const dim3 grid(num_splits, Hkv * head_slices, B);
   const float scale_log2 = scale * 1.4426950408889634f;
   decode_splitkv_kernel<D><<<grid, kWarps * 32, C::kSmemBytes, stream>>>(
-      tmK, tmV, static_cast<const __nv_bfloat16*>(q), o_part, lse_part, B, Hq, Hkv, Sk, chunk,
-      head_slices, scale_log2, status);
+      tmK, tmV, static_cast<const __nv_bfloat16*>(q), o_part, lse_part, seqlens, B, Hq, Hkv, Sk,
+      num_splits, head_slices, scale_log2, status);
   return cudaGetLastError();
 }
 
@@ -463,13 +479,13 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, floa
 
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
-                                  int num_splits, float scale, cudaStream_t stream,
-                                  int* status) {
+                                  int num_splits, float scale, cudaStream_t stream, int* status,
+                                  const int* seqlens) {
   if (D == 128)
-    return launch_decode_impl<128>(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, num_splits,
-                                   scale, stream, status);
-  return launch_decode_impl<64>(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, num_splits, scale,
-                                stream, status);
+    return launch_decode_impl<128>(q, k, v, seqlens, o_part, lse_part, B, Hq, Hkv, Sk,
+                                   num_splits, scale, stream, status);
+  return launch_decode_impl<64>(q, k, v, seqlens, o_part, lse_part, B, Hq, Hkv, Sk, num_splits,
+                                scale, stream, status);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,

@@ -32,10 +32,11 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, float* 
                             int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                             float scale, cudaStream_t stream, int* status);
 
+// seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
-                                  int num_splits, float scale, cudaStream_t stream,
-                                  int* status);
+                                  int num_splits, float scale, cudaStream_t stream, int* status,
+                                  const int* seqlens = nullptr);
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,
                            int rows, int D, int num_splits, cudaStream_t stream);

@@ -60,6 +60,23 @@ def dec(lib, q=A, k=A, v=A, op=A, lp=A, B=1, Hq=4, Hkv=1, Sk=64, D=128, ns=4, sc
     return lib.attn_decode_splitkv(q, k, v, op, lp, B, Hq, Hkv, Sk, D, ns, scale, None)
 
 
+def decv(lib, q=A, k=A, v=A, sl=A, op=A, lp=A, B=1, Hq=4, Hkv=1, Sk=64, D=128, ns=4, scale=0.1):
+    return lib.attn_decode_splitkv_varlen(q, k, v, sl, op, lp, B, Hq, Hkv, Sk, D, ns, scale,
+                                          None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(sl=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sl=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(v=M), attn.ATTN_ERR_MISALIGNED),
+])
+def test_decode_varlen_rejects(lib, kw, code):
+    assert decv(lib, **kw) == code
+
+
 def comb(lib, op=A, lp=A, o=A, lse=A, B=1, Hq=4, D=128, ns=4):
     return lib.attn_combine(op, lp, o, lse, B, Hq, D, ns, None)
 

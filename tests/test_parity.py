@@ -211,3 +211,37 @@ def test_decode_matches_prefill_kernel():
     of, lf = gpu_fwd(q, k, v, False, 0.09)
     assert np.max(np.abs(o - of[:, :, 0])) <= O_TOL
     assert np.max(np.abs(lse - lf[:, :, 0])) <= LSE_TOL * 10
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sk,D,ns", [
+    (6, 8, 2, 700, 128, 4),
+    (5, 4, 4, 300, 64, 3),
+    (4, 32, 8, 2048, 128, 8),
+])
+def test_decode_varlen(B, Hq, Hkv, Sk, D, ns):
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=B * 7 + Sk)
+    g = torch.Generator().manual_seed(Sk)
+    lens = torch.randint(0, Sk + 1, (B,), generator=g, dtype=torch.int32)
+    lens[0] = 0            # empty sequence
+    lens[1] = Sk           # full capacity
+    lens[2] = 1            # a single key
+    kd, vd = k.cuda(), v.cuda()
+    # Cache slots past each sequence's length hold NaN: they must not leak in.
+    for b in range(B):
+        kd[b, :, int(lens[b]):] = float("nan")
+        vd[b, :, int(lens[b]):] = float("nan")
+    scale = 1.0 / math.sqrt(D)
+    op, lp = attn.attn_decode_splitkv_varlen(q.cuda(), kd, vd, lens.cuda(), ns, scale)
+    o, lse = attn.attn_combine(op, lp)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    op, lp, o, lse = (t.cpu().numpy() for t in (op, lp, o, lse))
+    for b in range(B):
+        n = int(lens[b])
+        qb = q[b:b + 1].contiguous()
+        kb = k[b:b + 1, :, :n].contiguous()
+        vb = v[b:b + 1, :, :n].contiguous()
+        op_ref, lp_ref = oracle.decode_split(qb, kb, vb, ns, scale)
+        assert_close(op[:, b:b + 1], lp[:, b:b + 1], op_ref, lp_ref, f"partials b={b} len={n}")
+        o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, False, scale)
+        assert_close(o[b:b + 1], lse[b:b + 1], o_ref[:, :, 0], lse_ref[:, :, 0], f"b={b} len={n}")
