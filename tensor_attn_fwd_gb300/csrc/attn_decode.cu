@@ -384,6 +384,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       if (part == 0) lse_part[row] = lse;
     }
   }
+  // The combine kernel may now be scheduled; it waits for this grid to finish.
+  grid_launch_dependents();
 }
 
 // One warp per output row: lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
@@ -400,6 +402,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   constexpr float kLog2e = 1.4426950408889634f;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  // Launched as a dependent of the split kernel: its partials are complete
+  // and visible once this returns.
+  grid_dependency_wait();
   if (row >= rows) return;
   float M = -INFINITY;
   for (int s = lane; s < num_splits; s += 32)
@@ -490,11 +495,24 @@ cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, f
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,
                            int rows, int D, int num_splits, cudaStream_t stream) {
-  const dim3 grid((rows + 7) / 8);
+  // Programmatic stream serialisation: the combine grid is scheduled while the
+  // preceding split kernel drains and waits for it on the device.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + 7) / 8, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (D == 128)
-    combine_kernel<128><<<grid, 256, 0, stream>>>(o_part, lse_part, o, lse, rows, num_splits);
+    e = cudaLaunchKernelEx(&cfg, combine_kernel<128>, o_part, lse_part, o, lse, rows, num_splits);
   else
-    combine_kernel<64><<<grid, 256, 0, stream>>>(o_part, lse_part, o, lse, rows, num_splits);
+    e = cudaLaunchKernelEx(&cfg, combine_kernel<64>, o_part, lse_part, o, lse, rows, num_splits);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -361,6 +361,19 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- dependent launches
+// Let the next kernel in the stream (launched with programmatic stream
+// serialisation) start its prologue; it still waits for this grid's results.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding grid has completed and its memory is visible
+// (a no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- scalar math
 // 2^x on the special-function unit (approximate, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
