@@ -40,11 +40,12 @@ METRIC = "attn fwd TFLOP/s & % BF16 TC peak (prefill); decode HBM GB/s & % of pe
 PREFILL = WORKLOADS[3]
 DECODE = WORKLOADS[5]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per launch of the prefill kernel on the workload
-# above, from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`;
-# None until a capture of the current kernel exists (profiles/ holds the summary).
-PREFILL_TRAFFIC_BYTES = None
-DECODE_TRAFFIC_BYTES = None
+# DRAM bytes (read + write) per launch of each kernel on the workloads above,
+# from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (one pass) of
+# `bench.py --profile prefill|decode`; profiles/ holds the summary.  Reset to
+# None whenever the kernel changes until it is captured again.
+PREFILL_TRAFFIC_BYTES = 392657408 + 218246144
+DECODE_TRAFFIC_BYTES = 1074300160 + 10448384
 
 
 def load_peaks():

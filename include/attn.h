@@ -69,6 +69,17 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, float *o, flo
              void *stream);
 
 /*
+ * attn_fwd with a bf16 output: identical computation and arguments, except
+ * that o is [B,Hq,Sq,D] bf16 (each fp32 result rounded to nearest even),
+ * halving the output traffic.  LSE stays fp32.
+ * Source: as attn_fwd (the FlashAttention-style kernels the page compares
+ * against write their output in the input precision).
+ */
+ATTN_API int attn_fwd_bf16o(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                            float scale, void *stream);
+
+/*
  * Split-KV decode, first stage: per-split partial results for one query row
  * per head.  Source: same page, Methodology and Evaluation (FlashDecoding:
  * decode is GEMV plus softmax, memory bound, no tensor cores).

@@ -9,6 +9,7 @@ exception is raised.
 
 Names follow the C ABI:
     attn_fwd(q, k, v, causal, scale)            -> (o, lse)
+    attn_fwd_bf16o(q, k, v, causal, scale)      -> (o bf16, lse)
     attn_decode_splitkv(q, k, v, num_splits)    -> (o_part, lse_part)
     attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits) -> (o_part, lse_part)
     attn_combine(o_part, lse_part)              -> (o, lse)
@@ -24,7 +25,7 @@ import threading
 
 import torch
 
-__all__ = ["AttnError", "attn_fwd", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
+__all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
            "attn_combine", "decode",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
@@ -50,6 +51,8 @@ _flt = ctypes.c_float
 _SIGNATURES = {
     "attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _int, _flt,
                   _vp], _int),
+    "attn_fwd_bf16o": ([_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _int, _flt,
+                        _vp], _int),
     "attn_decode_splitkv": ([_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int,
                              _flt, _vp], _int),
     "attn_decode_splitkv_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
@@ -159,6 +162,34 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
                           lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
                           float(scale), _stream_handle(stream))
     _raise_if(st, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_bf16o(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                   scale: float | None = None, o: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, stream=None):
+    """attn_fwd with O returned in bf16 (LSE stays fp32)."""
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(k.device == q.device and v.device == q.device, "q/k/v must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty((B, Hq, Sq, D), dtype=torch.bfloat16, device=q.device)
+    _check(o.is_cuda and o.dtype == torch.bfloat16 and o.is_contiguous()
+           and tuple(o.shape) == (B, Hq, Sq, D) and o.device == q.device,
+           "o must be a contiguous bf16 CUDA tensor [B,Hq,Sq,D]")
+    lse = _out(lse, (B, Hq, Sq), q.device, "lse")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd_bf16o(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
+                                float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_fwd_bf16o")
     return o, lse
 
 

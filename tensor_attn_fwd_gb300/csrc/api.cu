@@ -148,8 +148,11 @@ const char* attn_status_string(int status) {
 
 int attn_version(void) { return (1 << 16) | 0; }
 
-int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq,
-             int Hkv, int Sq, int Sk, int D, int causal, float scale, void* stream) {
+namespace {
+
+int fwd_common(const void* q, const void* k, const void* v, void* o, int o_bf16, float* lse,
+               int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+               void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -166,9 +169,22 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
     return ATTN_ERR_MISALIGNED;
   int* status = status_word_device_ptr();
   if (status == nullptr) return ATTN_ERR_CUDA;
-  const cudaError_t e = launch_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale,
-                                        static_cast<cudaStream_t>(stream), status);
+  const cudaError_t e = launch_attn_fwd(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, D, causal,
+                                        scale, static_cast<cudaStream_t>(stream), status);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, int causal, float scale, void* stream) {
+  return fwd_common(q, k, v, o, 0, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream);
+}
+
+int attn_fwd_bf16o(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                   void* stream) {
+  return fwd_common(q, k, v, o, 1, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream);
 }
 
 namespace {

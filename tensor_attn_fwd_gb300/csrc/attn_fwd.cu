@@ -89,7 +89,8 @@ struct Bars {
 static_assert(sizeof(Bars) <= 256, "barrier block too large");
 
 struct FwdParams {
-  float* o;
+  void* o;           // fp32, or bf16 when o_bf16
+  int o_bf16;
   float* lse;
   int* status;
   int B, Hq, Hkv, Sq, Sk;
@@ -348,14 +349,22 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
     const int nt = it.n[t];
     const int row = it.q_row0 + 128 * t + quad * 32 + lane;
     const bool row_valid = row < p.Sq;
-    float* o_row = p.o + (static_cast<size_t>(it.bh) * p.Sq + row) * D;
+    const size_t o_off = (static_cast<size_t>(it.bh) * p.Sq + row) * D;
+    float* o_row = static_cast<float*>(p.o) + o_off;
+    __nv_bfloat16* o_row16 = static_cast<__nv_bfloat16*>(p.o) + o_off;
     float* lse_ptr = p.lse + static_cast<size_t>(it.bh) * p.Sq + row;
     if (nt == 0) {
       // No key visible to any row of this tile (or the tile is past Sq).
       if (row_valid) {
+        if (p.o_bf16) {
 #pragma unroll 4
-        for (int c = 0; c < D; c += 4)
-          *reinterpret_cast<float4*>(o_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < D; c += 8)
+            *reinterpret_cast<uint4*>(o_row16 + c) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+#pragma unroll 4
+          for (int c = 0; c < D; c += 4)
+            *reinterpret_cast<float4*>(o_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         *lse_ptr = -INFINITY;
       }
       continue;
@@ -483,11 +492,23 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
       uint32_t orow[32];
       tmem_ld32(tO + c, orow);
       if (row_valid) {
+        if (p.o_bf16) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(o_row + c + e) =
-              make_float4(__uint_as_float(orow[e]) * inv_l, __uint_as_float(orow[e + 1]) * inv_l,
-                          __uint_as_float(orow[e + 2]) * inv_l, __uint_as_float(orow[e + 3]) * inv_l);
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(orow[e]) * inv_l, __uint_as_float(orow[e + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(orow[e + 2]) * inv_l, __uint_as_float(orow[e + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(orow[e + 4]) * inv_l, __uint_as_float(orow[e + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(orow[e + 6]) * inv_l, __uint_as_float(orow[e + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(o_row16 + c + e) = w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(o_row + c + e) =
+                make_float4(__uint_as_float(orow[e]) * inv_l, __uint_as_float(orow[e + 1]) * inv_l,
+                            __uint_as_float(orow[e + 2]) * inv_l, __uint_as_float(orow[e + 3]) * inv_l);
+        }
       }
     }
     if (row_valid) *lse_ptr = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
@@ -568,9 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 template <int D>
-cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, float* o, float* lse,
-                            int B, int Hq, int Hkv, int Sq, int Sk, int causal, float scale,
-                            cudaStream_t stream, int* status) {
+cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o, int o_bf16,
+                            float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
+                            float scale, cudaStream_t stream, int* status) {
   using C = Cfg<D>;
   CUtensorMap tmQ, tmK, tmV;
   if (!encode_bf16_map(&tmQ, q, D, Sq, B * Hq, 128) || !encode_bf16_map(&tmK, k, D, Sk, B * Hkv, 128) ||
@@ -581,6 +602,7 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, float* 
   if (e != cudaSuccess) return e;
   FwdParams p;
   p.o = o;
+  p.o_bf16 = o_bf16;
   p.lse = lse;
   p.status = status;
   p.B = B;
@@ -599,13 +621,14 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, float* 
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
-                            int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, int o_bf16,
+                            float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                             float scale, cudaStream_t stream, int* status) {
   if (D == 128)
-    return launch_fwd_impl<128>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream,
-                                status);
-  return launch_fwd_impl<64>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream, status);
+    return launch_fwd_impl<128>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+                                stream, status);
+  return launch_fwd_impl<64>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream,
+                             status);
 }
 
 }  // namespace attn

@@ -28,8 +28,9 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int D, int rows, int pl
 
 // Kernel launchers; arguments are already validated.  Return cudaError_t of
 // the launch.
-cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
-                            int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+// o: fp32 [B,Hq,Sq,D], or bf16 when o_bf16 != 0.
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, int o_bf16,
+                            float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                             float scale, cudaStream_t stream, int* status);
 
 // seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).

@@ -245,3 +245,23 @@ def test_decode_varlen(B, Hq, Hkv, Sk, D, ns):
         assert_close(op[:, b:b + 1], lp[:, b:b + 1], op_ref, lp_ref, f"partials b={b} len={n}")
         o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, False, scale)
         assert_close(o[b:b + 1], lse[b:b + 1], o_ref[:, :, 0], lse_ref[:, :, 0], f"b={b} len={n}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal", [
+    (1, 2, 2, 128, 128, 64, False),
+    (2, 8, 2, 700, 700, 128, True),
+    (1, 4, 1, 300, 900, 128, True),
+])
+def test_bf16_output(B, Hq, Hkv, Sq, Sk, D, causal):
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Sk, D, seed=Sq + Sk)
+    scale = 1.0 / math.sqrt(D)
+    o16, lse = attn.attn_fwd_bf16o(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    o32, lse32 = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    assert o16.dtype == torch.bfloat16
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    assert_close(o16.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16 O")
+    # exactly the fp32 result rounded to nearest even
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(lse, lse32)
