@@ -63,6 +63,13 @@ def _load():
             lib.oracle_decode_split.restype = ctypes.c_int
             lib.oracle_combine.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _vp]
             lib.oracle_combine.restype = ctypes.c_int
+            lib.oracle_attn_fwd_f64.argtypes = [
+                _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dbl, _vp, _vp]
+            lib.oracle_attn_fwd_f64.restype = ctypes.c_int
+            lib.oracle_attn_bwd_f64.argtypes = [
+                _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dbl,
+                _vp, _vp, _vp]
+            lib.oracle_attn_bwd_f64.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -147,3 +154,43 @@ def combine(o_part, lse_part):
     if rc != 0:
         raise ValueError(f"oracle_combine failed ({rc})")
     return o, lse
+
+
+def _f64(x) -> np.ndarray:
+    """Contiguous float64 copy of a tensor/array (bf16 values widen exactly)."""
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.float64)
+    import torch
+    return x.detach().to("cpu").to(torch.float64).contiguous().numpy()
+
+
+def attn_fwd_f64(q, k, v, causal: bool, scale: float):
+    """Forward on double inputs: O [B,Hq,Sq,D] and LSE [B,Hq,Sq] (float64)."""
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    B, Hq, Sq, D = qd.shape
+    _, Hkv, Sk, _ = kd.shape
+    o = np.empty((B, Hq, Sq, D))
+    lse = np.empty((B, Hq, Sq))
+    rc = _load().oracle_attn_fwd_f64(_ptr(qd), _ptr(kd), _ptr(vd), B, Hq, Hkv, Sq, Sk, D,
+                                     int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_f64 failed ({rc})")
+    return o, lse
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float):
+    """Gradients (dQ, dK, dV) of sum(dO * O) for Q [B,Hq,Sq,D], K/V [B,Hkv,Sk,D] (float64)."""
+    qd, kd, vd, dod = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Sq, D = qd.shape
+    _, Hkv, Sk, _ = kd.shape
+    if dod.shape != qd.shape:
+        raise ValueError("dO must match Q")
+    dq = np.empty_like(qd)
+    dk = np.empty_like(kd)
+    dv = np.empty_like(vd)
+    rc = _load().oracle_attn_bwd_f64(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dod), B, Hq, Hkv, Sq, Sk,
+                                     D, int(bool(causal)), float(scale), _ptr(dq), _ptr(dk),
+                                     _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd_f64 failed ({rc})")
+    return dq, dk, dv

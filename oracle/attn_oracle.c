@@ -246,3 +246,153 @@ int oracle_combine(const double *o_part, const double *lse_part, int64_t R,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Attention backward (TEST INFRASTRUCTURE, like everything in this file).
+ *
+ * The gradient of O = softmax(S) V with S = scale * Q K^T (+ mask) for an
+ * upstream gradient dO, written out row by row from the chain rule:
+ *   P_ij  = exp(s_ij - LSE_i)                 (visible j only)
+ *   dV_j  = sum_i P_ij dO_i                   (summed over the group's heads)
+ *   dP_ij = dO_i . V_j
+ *   Delta_i = sum_j P_ij dP_ij
+ *   dS_ij = P_ij (dP_ij - Delta_i)
+ *   dQ_i  = scale * sum_j dS_ij K_j
+ *   dK_j  = scale * sum_i dS_ij Q_i           (summed over the group's heads)
+ * Inputs are doubles here (the Python side widens bf16 exactly), so that a
+ * finite-difference check can perturb them.
+ * ------------------------------------------------------------------------ */
+
+/* Forward on double inputs (same definition as oracle_attn_fwd_rows). */
+int oracle_attn_fwd_f64(const double *q, const double *k, const double *v, int64_t B,
+                        int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t D, int causal,
+                        double scale, double *o, double *lse)
+{
+    if (check_dims(B, Hq, Hkv, Sq, Sk, D)) return 1;
+    int64_t group = Hq / Hkv;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        if (s == NULL) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < B * Hq * Sq; ++r) {
+                int64_t i = r % Sq, bh = r / Sq, h = bh % Hq, b = bh / Hq;
+                int64_t g = h / group;
+                const double *qr = q + r * D;
+                const double *kh = k + (b * Hkv + g) * Sk * D;
+                const double *vh = v + (b * Hkv + g) * Sk * D;
+                int64_t n = visible_keys(i, Sq, Sk, causal);
+                double *orow = o + r * D;
+                if (n <= 0) {
+                    for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
+                    lse[r] = -INFINITY;
+                    continue;
+                }
+                for (int64_t j = 0; j < n; ++j) {
+                    double acc = 0.0;
+                    for (int64_t d = 0; d < D; ++d) acc += qr[d] * kh[j * D + d];
+                    s[j] = scale * acc;
+                }
+                double m = s[0];
+                for (int64_t j = 1; j < n; ++j)
+                    if (s[j] > m) m = s[j];
+                double l = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    s[j] = exp(s[j] - m);
+                    l += s[j];
+                }
+                for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
+                for (int64_t j = 0; j < n; ++j)
+                    for (int64_t d = 0; d < D; ++d) orow[d] += s[j] * vh[j * D + d];
+                for (int64_t d = 0; d < D; ++d) orow[d] /= l;
+                lse[r] = m + log(l);
+            }
+        }
+        free(s);
+    }
+    return bad;
+}
+
+/* Backward.  q, dO: [B,Hq,Sq,D]; k, v: [B,Hkv,Sk,D] (doubles).
+ * dq: [B,Hq,Sq,D]; dk, dv: [B,Hkv,Sk,D] (overwritten). */
+int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const double *dout,
+                        int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t D,
+                        int causal, double scale, double *dq, double *dk, double *dv)
+{
+    if (check_dims(B, Hq, Hkv, Sq, Sk, D)) return 1;
+    int64_t group = Hq / Hkv;
+    int bad = 0;
+    for (int64_t t = 0; t < B * Hkv * Sk * D; ++t) {
+        dk[t] = 0.0;
+        dv[t] = 0.0;
+    }
+    /* One KV head per task: its dK/dV rows are owned by exactly one thread. */
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        if (p == NULL || dp == NULL) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bg = 0; bg < B * Hkv; ++bg) {
+                int64_t b = bg / Hkv, g = bg % Hkv;
+                const double *kh = k + bg * Sk * D;
+                const double *vh = v + bg * Sk * D;
+                double *dkh = dk + bg * Sk * D;
+                double *dvh = dv + bg * Sk * D;
+                for (int64_t h = g * group; h < (g + 1) * group; ++h) {
+                    int64_t bh = b * Hq + h;
+                    for (int64_t i = 0; i < Sq; ++i) {
+                        const double *qr = q + (bh * Sq + i) * D;
+                        const double *dor = dout + (bh * Sq + i) * D;
+                        double *dqr = dq + (bh * Sq + i) * D;
+                        for (int64_t d = 0; d < D; ++d) dqr[d] = 0.0;
+                        int64_t n = visible_keys(i, Sq, Sk, causal);
+                        if (n <= 0) continue;
+                        /* P row */
+                        for (int64_t j = 0; j < n; ++j) {
+                            double acc = 0.0;
+                            for (int64_t d = 0; d < D; ++d) acc += qr[d] * kh[j * D + d];
+                            p[j] = scale * acc;
+                        }
+                        double m = p[0];
+                        for (int64_t j = 1; j < n; ++j)
+                            if (p[j] > m) m = p[j];
+                        double l = 0.0;
+                        for (int64_t j = 0; j < n; ++j) {
+                            p[j] = exp(p[j] - m);
+                            l += p[j];
+                        }
+                        for (int64_t j = 0; j < n; ++j) p[j] /= l;
+                        /* dP row and Delta */
+                        double delta = 0.0;
+                        for (int64_t j = 0; j < n; ++j) {
+                            double acc = 0.0;
+                            for (int64_t d = 0; d < D; ++d) acc += dor[d] * vh[j * D + d];
+                            dp[j] = acc;
+                            delta += p[j] * acc;
+                        }
+                        /* dS and the three products */
+                        for (int64_t j = 0; j < n; ++j) {
+                            double ds = p[j] * (dp[j] - delta);
+                            for (int64_t d = 0; d < D; ++d) {
+                                dqr[d] += scale * ds * kh[j * D + d];
+                                dkh[j * D + d] += scale * ds * qr[d];
+                                dvh[j * D + d] += p[j] * dor[d];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return bad;
+}
