@@ -133,6 +133,26 @@ ATTN_API int attn_decode_splitkv_varlen(const void *q, const void *k, const void
 ATTN_API int attn_combine(const float *o_part, const float *lse_part, float *o, float *lse, int B,
                  int Hq, int D, int num_splits, void *stream);
 
+/*
+ * Attention backward: gradients of sum(dO * O) for the attn_fwd computation.
+ * Source: "A Thread-Register Decoupled GPU Execution Model for Efficient
+ * Tensor Computation", Methodology and Evaluation (the FlashAttention backward
+ * pass: recompute the scores, then dV = P^T dO, dS = P * (dO V^T - Delta),
+ * dQ = scale * dS K, dK = scale * dS^T Q, with Delta = rowsum(dO * O)).
+ * dK and dV sum over the query heads that share a KV head.
+ *
+ *   q [B,Hq,Sq,D], k, v [B,Hkv,Sk,D], dout [B,Hq,Sq,D]   bf16
+ *   o [B,Hq,Sq,D] fp32 and lse [B,Hq,Sq] fp32            as written by attn_fwd
+ *   dq [B,Hq,Sq,D], dk, dv [B,Hkv,Sk,D]                  fp32 outputs
+ *   delta_ws [B,Hq,Sq] fp32                              caller-owned workspace
+ *   Same causal / scale / size rules as attn_fwd; D in {64, 128}.
+ * Enqueues three kernels (Delta, dK/dV, dQ) on `stream`.
+ */
+ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const float *o,
+                      const float *lse, const void *dout, float *dq, float *dk, float *dv,
+                      float *delta_ws, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                      float scale, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 ATTN_API const char *attn_status_string(int status);
 

@@ -14,6 +14,7 @@ Names follow the C ABI:
     attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits) -> (o_part, lse_part)
     attn_combine(o_part, lse_part)              -> (o, lse)
     decode(q, k, v, num_splits)                 -> (o, lse)   both stages
+    attn_bwd(q, k, v, o, lse, dout, causal, scale) -> (dq, dk, dv)
 Layouts: Q [B,Hq,Sq,D], K/V [B,Hkv,Sk,D] bf16; O [B,Hq,Sq,D], LSE [B,Hq,Sq] fp32.
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ import threading
 import torch
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
-           "attn_combine", "decode",
+           "attn_combine", "decode", "attn_bwd",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
            "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
@@ -58,6 +59,7 @@ _SIGNATURES = {
     "attn_decode_splitkv_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
                                     _int, _flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
+    "attn_bwd": ([_vp] * 10 + [_int] * 7 + [_flt, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
     "attn_debug_status": ([_vp], _int),
     "attn_version": ([], _int),
@@ -290,3 +292,40 @@ def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
         o_part, lse_part = attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits, scale,
                                                       o_part, lse_part, stream)
     return attn_combine(o_part, lse_part, o, lse, stream)
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, causal: bool = False,
+             scale: float | None = None, dq: torch.Tensor | None = None,
+             dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+             delta_ws: torch.Tensor | None = None, stream=None):
+    """Gradients of sum(dout * O) for O = attn_fwd(q, k, v): returns (dq, dk, dv) fp32.
+
+    o and lse are attn_fwd's fp32 outputs; dout is bf16 like q.
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    _check_bf16("dout", dout, 4)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(tuple(dout.shape) == tuple(q.shape), "dout must match q")
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _check(t.device == q.device, f"{name} must be on {q.device}")
+    o = _out(o, (B, Hq, Sq, D), q.device, "o")
+    lse = _out(lse, (B, Hq, Sq), q.device, "lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = _out(dq, (B, Hq, Sq, D), q.device, "dq")
+    dk = _out(dk, (B, Hkv, Sk, D), q.device, "dk")
+    dv = _out(dv, (B, Hkv, Sk, D), q.device, "dv")
+    delta_ws = _out(delta_ws, (B, Hq, Sq), q.device, "delta_ws")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          delta_ws.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
+                          float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_bwd")
+    return dq, dk, dv

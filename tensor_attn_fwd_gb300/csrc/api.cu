@@ -233,6 +233,35 @@ int attn_decode_splitkv_varlen(const void* q, const void* k, const void* v, cons
                        stream);
 }
 
+int attn_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
+             const void* dout, float* dq, float* dk, float* dv, float* delta_ws, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !delta_ws)
+    return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Sq > kMaxSeq || Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * Sq * D > kMaxElems ||
+      static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * ((Sq + 127) / 128) > (1ll << 30) ||
+      static_cast<long long>(B) * Hkv * ((Sk + 127) / 128) > (1ll << 30))
+    return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(delta_ws))
+    return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const cudaError_t e =
+      launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta_ws, B, Hq, Hkv, Sq, Sk, D, causal,
+                      scale, static_cast<cudaStream_t>(stream), status);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_combine(const float* o_part, const float* lse_part, float* o, float* lse, int B, int Hq,
                  int D, int num_splits, void* stream) {
   if (!o_part || !lse_part || !o || !lse) return ATTN_ERR_INVALID_ARG;

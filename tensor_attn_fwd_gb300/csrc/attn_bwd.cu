@@ -1,0 +1,614 @@
+// attn_bwd.cu -- attention backward (dQ, dK, dV) on sm_103a tensor cores.
+//
+// Source: "A Thread-Register Decoupled GPU Execution Model for Efficient Tensor
+// Computation", Methodology and Evaluation (the FlashAttention backward: more
+// GEMMs than the forward, more live tensors, operand transposes and score
+// recomputation).  For O = softmax(S) V with S = scale * Q K^T (+ mask) and an
+// upstream gradient dO:
+//   P = exp(S - LSE)   Delta_i = sum_d dO_id O_id   dP = dO V^T
+//   dS = P * (dP - Delta)   dV = P^T dO   dK = scale * dS^T Q   dQ = scale * dS K
+// (dK and dV sum over the query heads that share a KV head).
+//
+// Three kernels, enqueued in order on the caller's stream:
+//   delta kernel  Delta = rowsum(dO * O) into caller workspace.
+//   dK/dV kernel  one CTA per 128-key tile of one KV head.  It loops over every
+//                 (query head of the group, 128-row query tile) that sees those
+//                 keys: S^T = K Q^T and dP^T = V dO^T (smem x smem) into TMEM;
+//                 the gradient warps (one thread per key) turn them into P^T
+//                 and dS^T (bf16, written back into TMEM over S^T / dP^T); then
+//                 dV += P^T dO and dK += dS^T Q accumulate in TMEM.  No atomics.
+//   dQ kernel     one CTA per 128-row query tile: S = Q K^T and dP = dO V^T
+//                 recomputed for each visible KV tile, dS written into TMEM,
+//                 dQ += dS K accumulated in TMEM.
+// Roles (192 threads): warps 0-3 gradient math, warp 4 MMA issue, warp 5 TMA.
+// The Q/dO (dK/dV kernel) or K/V (dQ kernel) tiles stream through a two-stage
+// ring; the fixed operand tiles are loaded once.  All waits are bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdMmaWarp = 4;
+constexpr int kBwdLoadWarp = 5;
+constexpr int kStages = 2;
+constexpr uint32_t kSub = 128 * 128;  // [128 rows x 64 bf16] 128B-swizzled sub-tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr uint32_t kTile = (D / 64) * kSub;  // one 128 x D bf16 tile
+  // smem: two fixed tiles, kStages x (two streamed tiles), then scalars/barriers
+  static constexpr uint32_t kFixed = 2 * kTile;
+  static constexpr uint32_t kRing = kStages * 2 * kTile;
+  // Per gradient warp, two buffers of (LSE2[128], Delta[128]) for the current step.
+  static constexpr uint32_t kScalars = 4 * 2 * 2 * 128 * 4;
+  static constexpr uint32_t kBarBytes = 256;
+  static constexpr size_t kSmem = 1024 + kFixed + kRing + kScalars + kBarBytes;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 256 + D;
+  static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, false, true);
+};
+
+struct BwdBars {
+  uint64_t fixed_full;
+  uint64_t full[kStages], empty[kStages];
+  uint64_t sd_full;   // S and dP of the current step are in TMEM
+  uint64_t p_full;    // P / dS of the current step are in TMEM
+  uint64_t acc_full;  // all accumulating MMAs have completed
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct BwdParams {
+  const float* lse;    // [B,Hq,Sq] natural log
+  const float* delta;  // [B,Hq,Sq]
+  float* out0;         // dkdv: dK [B,Hkv,Sk,D]; dq: dQ [B,Hq,Sq,D]
+  float* out1;         // dkdv: dV
+  int* status;
+  int B, Hq, Hkv, Sq, Sk, causal;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ void bwd_record(int* status) {
+  if (status != nullptr) atomicCAS(status, 0, ATTN_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, BwdBars* bars) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&bars->abort)) return false;
+    if (globaltimer() - t0 > ATTN_WAIT_NS) {
+      *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+      return false;
+    }
+  }
+}
+
+// First 128-row query tile that can see key tile n (bottom-right causal).
+__device__ __forceinline__ int first_q_tile(const BwdParams& p, int n) {
+  if (!p.causal) return 0;
+  const int row = 128 * n - (p.Sk - p.Sq);
+  return row <= 0 ? 0 : row / 128;
+}
+
+// KV tiles a query tile needs (as in the forward).
+__device__ __forceinline__ int kv_tiles_for(const BwdParams& p, int m) {
+  const int row_first = 128 * m;
+  if (row_first >= p.Sq) return 0;
+  int nvis = p.Sk;
+  if (p.causal) {
+    const int row_last = min(row_first + 127, p.Sq - 1);
+    nvis = min(p.Sk, row_last + p.Sk - p.Sq + 1);
+    if (nvis <= 0) return 0;
+  }
+  return (nvis + 127) / 128;
+}
+
+// ------------------------------------------------------------------ Delta
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ dout,
+                                                        const float* __restrict__ o,
+                                                        float* __restrict__ delta, int rows) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int DPL = D / 32;
+  const __nv_bfloat16* dr = dout + static_cast<size_t>(row) * D + lane * DPL;
+  const float* orow = o + static_cast<size_t>(row) * D + lane * DPL;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc = fmaf(__bfloat162float(dr[e]), orow[e], acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// ------------------------------------------------------------------ shared pieces
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                          int row0, int plane) {
+#pragma unroll
+  for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * kSub, map, bar, s * 64, row0, plane);
+}
+
+// Two 128x128 SS products into TMEM: d0 = a0 b0^T, d1 = a1 b1^T (K-major tiles).
+template <int D>
+__device__ __forceinline__ void mma_two_ss(uint32_t tmem, uint32_t a0, uint32_t b0, uint32_t a1,
+                                           uint32_t b1) {
+  using C = BwdCfg<D>;
+  constexpr uint64_t kDesc = sdesc_sw128(0, 16, 1024);
+  constexpr uint32_t kHi = static_cast<uint32_t>(kDesc >> 32);
+  constexpr uint32_t kLo = static_cast<uint32_t>(kDesc);
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t a = kLo + ((which ? a1 : a0) >> 4);
+    const uint32_t b = kLo + ((which ? b1 : b0) >> 4);
+    const uint32_t d = tmem + (which ? C::kColDP : C::kColS);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * kSub + (kk & 3) * 32) >> 4;
+      const uint64_t ad = desc_from_words(a + off, kHi);
+      const uint64_t bd = desc_from_words(b + off, kHi);
+      if (kk == 0)
+        mma_ss_c<0>(d, ad, bd, C::kIdescSS);
+      else
+        mma_ss_c<1>(d, ad, bd, C::kIdescSS);
+    }
+  }
+}
+
+// acc (+)= A(tmem, 128 x 128 bf16 at column a_col) x B(smem tile, MN-major).
+template <int D>
+__device__ __forceinline__ void mma_ts_acc(uint32_t tmem, uint32_t acc_col, uint32_t a_col,
+                                           uint32_t b_smem, bool first) {
+  using C = BwdCfg<D>;
+  constexpr uint64_t kDesc = sdesc_sw128(0, kSub, 1024);
+  constexpr uint32_t kHi = static_cast<uint32_t>(kDesc >> 32);
+  constexpr uint32_t kLo = static_cast<uint32_t>(kDesc);
+  const uint32_t b = kLo + (b_smem >> 4);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t bd = desc_from_words(b + kk * (2048 >> 4), kHi);
+    if (first && kk == 0)
+      mma_ts_c<0>(tmem + acc_col, tmem + a_col + kk * 8, bd, C::kIdescTS);
+    else
+      mma_ts_c<1>(tmem + acc_col, tmem + a_col + kk * 8, bd, C::kIdescTS);
+  }
+}
+
+// Read a 128-column fp32 accumulator row of this thread from TMEM, scale it and
+// store it to global memory (valid rows only).
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float* dst, float mul, bool valid) {
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c, r);
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(dst + c + e) =
+            make_float4(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul,
+                        __uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dK / dV
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kTile;
+  uint8_t* sRing = smem + C::kFixed;  // stage st: Q at +0, dO at +kTile
+  float* sScal = reinterpret_cast<float*>(smem + C::kFixed + C::kRing);  // [st][2][128]
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kFixed + C::kRing + C::kScalars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Work: key tile n of KV head (b, g); CTAs are numbered n-major so the
+  // largest work (low n under a causal mask) is scheduled first.
+  const int n = blockIdx.x / (p.B * p.Hkv);
+  const int bg = blockIdx.x % (p.B * p.Hkv);
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int group = p.Hq / p.Hkv;
+  const int mtiles = (p.Sq + 127) / 128;
+  const int m0 = min(first_q_tile(p, n), mtiles);
+  const int per_head = mtiles - m0;
+  const int nsteps = group * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->fixed_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->sd_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  bool ok = true;
+
+  if (warp == kBwdLoadWarp) {
+    if (lane == 0 && nsteps > 0) {
+      mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
+      load_tile<D>(sK, &tmK, &bars->fixed_full, 128 * n, bg);
+      load_tile<D>(sV, &tmV, &bars->fixed_full, 128 * n, bg);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int st = s % kStages;
+        if (s >= kStages && !(ok = bwd_wait(&bars->empty[st], ((s / kStages) - 1) & 1, bars)))
+          break;
+        const int h = g * group + s / per_head;
+        const int m = m0 + s % per_head;
+        uint8_t* dst = sRing + st * 2 * C::kTile;
+        mbar_arrive_expect_tx(&bars->full[st], 2 * C::kTile);
+        load_tile<D>(dst, &tmQ, &bars->full[st], 128 * m, b * p.Hq + h);
+        load_tile<D>(dst + C::kTile, &tmDO, &bars->full[st], 128 * m, b * p.Hq + h);
+      }
+      if (!ok) bwd_record(p.status);
+      for (int s = max(0, nsteps - kStages); s < nsteps; ++s)
+        (void)mbar_wait(&bars->full[s % kStages], (s / kStages) & 1);
+      (void)mbar_wait(&bars->fixed_full, 0);
+    }
+  } else if (warp == kBwdMmaWarp) {
+    if (lane == 0 && nsteps > 0) {
+      ok = bwd_wait(&bars->fixed_full, 0, bars);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int st = s % kStages;
+        if (!(ok = bwd_wait(&bars->full[st], (s / kStages) & 1, bars))) break;
+        const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
+        const uint32_t do_addr = q_addr + C::kTile;
+        // S^T = K Q^T and dP^T = V dO^T
+        mma_two_ss<D>(tmem, k_addr, q_addr, v_addr, do_addr);
+        tc_commit(&bars->sd_full);
+        if (!(ok = bwd_wait(&bars->p_full, s & 1, bars))) break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q (B operands MN-major: rows are the K dim)
+        mma_ts_acc<D>(tmem, C::kColA1, C::kColS, do_addr, s == 0);
+        mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, q_addr, s == 0);
+        tc_commit(&bars->empty[st]);
+      }
+      if (ok) tc_commit(&bars->acc_full);
+      if (!ok) bwd_record(p.status);
+      tc_commit(&bars->mma_done);
+      (void)mbar_wait(&bars->mma_done, 0);
+    }
+  } else {
+    // Gradient warps: thread r owns key 128n + r (TMEM lane r).
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const int key = 128 * n + r;
+    const bool key_valid = key < p.Sk;
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int h = g * group + s / per_head;
+      const int m = m0 + s % per_head;
+      const int bh = b * p.Hq + h;
+      // This step's per-row LSE (log2 domain) and Delta in the warp's own
+      // buffer (no cross-warp barrier, so an aborting warp cannot strand others).
+      float* lse2 = sScal + (quad * 2 + (s & 1)) * 256;
+      float* dlt = lse2 + 128;
+      for (int t = lane; t < 128; t += 32) {
+        const int row = 128 * m + t;
+        const bool rv = row < p.Sq;
+        lse2[t] = rv ? __ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e : 0.f;
+        dlt[t] = rv ? __ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
+      }
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->sd_full, s & 1, bars));
+      if (!ok) break;
+      tc_fence_after();
+      // Visible rows for this key: row >= key - (Sk - Sq) (causal) and row < Sq.
+      const int row_lo = p.causal ? key - (p.Sk - p.Sq) : -0x40000000;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_addr + C::kColS + 32 * c, sr);
+        tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 32 * c + e + u;
+            const int row = 128 * m + col;
+            const bool vis = key_valid && row < p.Sq && row >= row_lo;
+            const float x = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -lse2[col]);
+            pv[u] = vis ? ex2(x) : 0.f;
+            dv[u] = pv[u] * (__uint_as_float(dr[e + u]) - dlt[col]);
+          }
+          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+          dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_st16(tmem + lane_addr + C::kColS + 16 * c, pk);
+        tmem_st16(tmem + lane_addr + C::kColDP + 16 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+    }
+    if (ok) {
+      float* dk_row = p.out0 + (static_cast<size_t>(bg) * p.Sk + key) * D;
+      float* dv_row = p.out1 + (static_cast<size_t>(bg) * p.Sk + key) * D;
+      if (nsteps == 0) {
+        // No query row sees these keys: their gradients are zero.
+        if (key_valid) {
+          for (int c = 0; c < D; c += 4) {
+            *reinterpret_cast<float4*>(dk_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(dv_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      } else {
+        ok = __all_sync(0xffffffffu, bwd_wait(&bars->acc_full, 0, bars));
+        if (ok) {
+          tc_fence_after();
+          store_acc_row<D>(tmem + lane_addr + C::kColA0, dk_row, p.scale, key_valid);
+          store_acc_row<D>(tmem + lane_addr + C::kColA1, dv_row, 1.f, key_valid);
+        }
+      }
+    }
+    if (!ok) bwd_record(p.status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::kTile;
+  uint8_t* sRing = smem + C::kFixed;  // stage st: K at +0, V at +kTile
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kFixed + C::kRing + C::kScalars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Work: query tile m of head (b, h); CTAs are numbered m-major, highest m
+  // (largest work under a causal mask) first.
+  const int mtiles = (p.Sq + 127) / 128;
+  const int m = mtiles - 1 - static_cast<int>(blockIdx.x / (p.B * p.Hq));
+  const int bh = blockIdx.x % (p.B * p.Hq);
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int nsteps = kv_tiles_for(p, m);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->fixed_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->sd_full, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  bool ok = true;
+
+  if (warp == kBwdLoadWarp) {
+    if (lane == 0 && nsteps > 0) {
+      mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
+      load_tile<D>(sQ, &tmQ, &bars->fixed_full, 128 * m, bh);
+      load_tile<D>(sDO, &tmDO, &bars->fixed_full, 128 * m, bh);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int st = s % kStages;
+        if (s >= kStages && !(ok = bwd_wait(&bars->empty[st], ((s / kStages) - 1) & 1, bars)))
+          break;
+        uint8_t* dst = sRing + st * 2 * C::kTile;
+        mbar_arrive_expect_tx(&bars->full[st], 2 * C::kTile);
+        load_tile<D>(dst, &tmK, &bars->full[st], 128 * s, bkv);
+        load_tile<D>(dst + C::kTile, &tmV, &bars->full[st], 128 * s, bkv);
+      }
+      if (!ok) bwd_record(p.status);
+      for (int s = max(0, nsteps - kStages); s < nsteps; ++s)
+        (void)mbar_wait(&bars->full[s % kStages], (s / kStages) & 1);
+      (void)mbar_wait(&bars->fixed_full, 0);
+    }
+  } else if (warp == kBwdMmaWarp) {
+    if (lane == 0 && nsteps > 0) {
+      ok = bwd_wait(&bars->fixed_full, 0, bars);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int st = s % kStages;
+        if (!(ok = bwd_wait(&bars->full[st], (s / kStages) & 1, bars))) break;
+        const uint32_t k_addr = smem_u32(sRing + st * 2 * C::kTile);
+        const uint32_t v_addr = k_addr + C::kTile;
+        // S = Q K^T and dP = dO V^T
+        mma_two_ss<D>(tmem, q_addr, k_addr, do_addr, v_addr);
+        tc_commit(&bars->sd_full);
+        if (!(ok = bwd_wait(&bars->p_full, s & 1, bars))) break;
+        tc_fence_after();
+        // dQ += dS K (K MN-major: its rows are the K dim)
+        mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, k_addr, s == 0);
+        tc_commit(&bars->empty[st]);
+      }
+      if (ok) tc_commit(&bars->acc_full);
+      if (!ok) bwd_record(p.status);
+      tc_commit(&bars->mma_done);
+      (void)mbar_wait(&bars->mma_done, 0);
+    }
+  } else {
+    // Gradient warps: thread r owns query row 128m + r (TMEM lane r).
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    const int row = 128 * m + r;
+    const bool row_valid = row < p.Sq;
+    const float lse2 = row_valid ? __ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e
+                                 : 0.f;
+    const float dlt = row_valid ? __ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
+    const int key_hi = p.causal ? min(p.Sk - 1, row + p.Sk - p.Sq) : p.Sk - 1;
+    for (int s = 0; s < nsteps && ok; ++s) {
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->sd_full, s & 1, bars));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_addr + C::kColS + 32 * c, sr);
+        tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int key = 128 * s + 32 * c + e + u;
+            const bool vis = row_valid && key <= key_hi;
+            const float x = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -lse2);
+            const float pv = vis ? ex2(x) : 0.f;
+            dv[u] = pv * (__uint_as_float(dr[e + u]) - dlt);
+          }
+          dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_st16(tmem + lane_addr + C::kColDP + 16 * c, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+    }
+    if (ok) {
+      float* dq_row = p.out0 + (static_cast<size_t>(bh) * p.Sq + row) * D;
+      if (nsteps == 0) {
+        if (row_valid)
+          for (int c = 0; c < D; c += 4)
+            *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        ok = __all_sync(0xffffffffu, bwd_wait(&bars->acc_full, 0, bars));
+        if (ok) {
+          tc_fence_after();
+          store_acc_row<D>(tmem + lane_addr + C::kColA0, dq_row, p.scale, row_valid);
+        }
+      }
+    }
+    if (!ok) bwd_record(p.status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_impl(const void* q, const void* k, const void* v, const float* o,
+                            const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                            float* delta, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
+                            float scale, cudaStream_t stream, int* status) {
+  using C = BwdCfg<D>;
+  const int rows = B * Hq * Sq;
+  bwd_delta_kernel<D><<<(rows + 7) / 8, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(dout), o, delta, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap tmQ, tmK, tmV, tmDO;
+  if (!encode_bf16_map(&tmQ, q, D, Sq, B * Hq, 128) ||
+      !encode_bf16_map(&tmK, k, D, Sk, B * Hkv, 128) ||
+      !encode_bf16_map(&tmV, v, D, Sk, B * Hkv, 128) ||
+      !encode_bf16_map(&tmDO, dout, D, Sq, B * Hq, 128))
+    return cudaErrorInvalidValue;
+  if ((e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dkdv_kernel<D>),
+                            static_cast<int>(C::kSmem))) != cudaSuccess)
+    return e;
+  if ((e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dq_kernel<D>),
+                            static_cast<int>(C::kSmem))) != cudaSuccess)
+    return e;
+  BwdParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.out0 = dk;
+  p.out1 = dv;
+  const int kv_ctas = B * Hkv * ((Sk + 127) / 128);
+  bwd_dkdv_kernel<D><<<kv_ctas, kBwdThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, tmDO, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  p.out0 = dq;
+  p.out1 = nullptr;
+  const int q_ctas = B * Hq * ((Sq + 127) / 128);
+  bwd_dq_kernel<D><<<q_ctas, kBwdThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, tmDO, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const float* o,
+                            const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                            float* delta, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                            int causal, float scale, cudaStream_t stream, int* status) {
+  if (D == 128)
+    return launch_bwd_impl<128>(q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, Sq, Sk,
+                                causal, scale, stream, status);
+  return launch_bwd_impl<64>(q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, Sq, Sk, causal,
+                             scale, stream, status);
+}
+
+}  // namespace attn

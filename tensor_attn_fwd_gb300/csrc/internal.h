@@ -39,6 +39,12 @@ cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, f
                                   int num_splits, float scale, cudaStream_t stream, int* status,
                                   const int* seqlens = nullptr);
 
+// Backward: Delta into `delta` ([B,Hq,Sq]), then dK/dV and dQ kernels.
+cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const float* o,
+                            const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                            float* delta, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                            int causal, float scale, cudaStream_t stream, int* status);
+
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,
                            int rows, int D, int num_splits, cudaStream_t stream);
 
