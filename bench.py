@@ -320,6 +320,33 @@ def ours_arm(args, rank, world, local_rank, dist_on):
                      "peak_source": f"{peaks_src} STREAM-style copy"},
     }
 
+    # ---------------- backward on the prefill workload (Delta + dK/dV + dQ kernels)
+    backward = None
+    if not args.no_backward:
+        g = torch.Generator().manual_seed(w.seed + 7)
+        dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(device)
+        dq = torch.empty(q.shape, dtype=torch.float32, device=device)
+        dk = torch.empty(k.shape, dtype=torch.float32, device=device)
+        dv = torch.empty(v.shape, dtype=torch.float32, device=device)
+        dws = torch.empty(lse.shape, dtype=torch.float32, device=device)
+        prefill()
+
+        def bwd():
+            attn.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
+                          dv=dv, delta_ws=dws, stream=stream)
+
+        b_steps = max(3, min(args.steps, 50))
+        b_times = time_launches(bwd, b_steps, 3, flush_buf, stream)
+        b_ms = sum(b_times) / len(b_times)
+        b_flops = 2.5 * flops  # five GEMM-sized products against the forward's two
+        backward = {"workload": w.name, "metric": "attn bwd TFLOP/s (2.5x forward FLOPs)",
+                    "value": b_flops / (b_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": b_ms, "steps": b_steps,
+                    "frac_of_measured_bf16_peak": b_flops / (b_ms * 1e-3) / 1e12
+                    / peaks["bf16_tflops"],
+                    "gpu_launches_per_step": 3}
+        del dq, dk, dv, dws, dout
+
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.no_e2e:
@@ -370,6 +397,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
                      "traffic": PREFILL_TRAFFIC_BYTES,
                      "peak_source": f"{peaks_src} cuBLAS bf16 burst"},
         "decode": decode,
+        "backward": backward,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": args.steps,
@@ -413,6 +441,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
                     help="run a few launches of one kernel (for ncu) and exit")
