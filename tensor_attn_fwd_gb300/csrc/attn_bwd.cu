@@ -20,7 +20,11 @@
 //   dQ kernel     one CTA per 128-row query tile: S = Q K^T and dP = dO V^T
 //                 recomputed for each visible KV tile, dS written into TMEM,
 //                 dQ += dS K accumulated in TMEM.
-// Roles (192 threads): warps 0-3 gradient math, warp 4 MMA issue, warp 5 TMA.
+// Roles (320 threads): warps 0-7 gradient math (two warpgroups, each owning 64
+// of a tile's 128 columns: the backward needs no row reductions, so the split
+// is free), warp 8 MMA issue, warp 9 TMA.  Each warpgroup writes its bf16
+// P / dS values into its own half of the S / dP columns, so neither can
+// overwrite scores the other has not read yet.
 // The Q/dO (dK/dV kernel) or K/V (dQ kernel) tiles stream through a two-stage
 // ring; the fixed operand tiles are loaded once.  All waits are bounded.
 #include <cuda.h>
@@ -38,9 +42,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdMmaWarp = 4;
-constexpr int kBwdLoadWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdMmaWarp = 8;
+constexpr int kBwdLoadWarp = 9;
+constexpr int kGradThreads = 256;
 constexpr int kStages = 2;
 constexpr uint32_t kSub = 128 * 128;  // [128 rows x 64 bf16] 128B-swizzled sub-tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -52,7 +57,7 @@ struct BwdCfg {
   static constexpr uint32_t kFixed = 2 * kTile;
   static constexpr uint32_t kRing = kStages * 2 * kTile;
   // Per gradient warp, two buffers of (LSE2[128], Delta[128]) for the current step.
-  static constexpr uint32_t kScalars = 4 * 2 * 2 * 128 * 4;
+  static constexpr uint32_t kScalars = 8 * 2 * 2 * 128 * 4;
   static constexpr uint32_t kBarBytes = 256;
   static constexpr size_t kSmem = 1024 + kFixed + kRing + kScalars + kBarBytes;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 256 + D;
@@ -186,19 +191,22 @@ __device__ __forceinline__ void mma_ts_acc(uint32_t tmem, uint32_t acc_col, uint
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint64_t bd = desc_from_words(b + kk * (2048 >> 4), kHi);
+    // bf16 A: rows 0-63 packed at columns [0,32), rows 64-127 at [64,96).
+    const uint32_t ac = a_col + kk * 8 + (kk >= 4 ? 32 : 0);
     if (first && kk == 0)
-      mma_ts_c<0>(tmem + acc_col, tmem + a_col + kk * 8, bd, C::kIdescTS);
+      mma_ts_c<0>(tmem + acc_col, tmem + ac, bd, C::kIdescTS);
     else
-      mma_ts_c<1>(tmem + acc_col, tmem + a_col + kk * 8, bd, C::kIdescTS);
+      mma_ts_c<1>(tmem + acc_col, tmem + ac, bd, C::kIdescTS);
   }
 }
 
 // Read a 128-column fp32 accumulator row of this thread from TMEM, scale it and
 // store it to global memory (valid rows only).
 template <int D>
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, float* dst, float mul, bool valid) {
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float* dst, float mul, bool valid,
+                                              int c_begin, int c_end) {
 #pragma unroll 1
-  for (int c = 0; c < D; c += 32) {
+  for (int c = c_begin; c < c_end; c += 32) {
     uint32_t r[32];
     tmem_ld32(taddr + c, r);
     if (valid) {
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->empty[s], 1);
     }
     mbar_init(&bars->sd_full, 1);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_full, kGradThreads);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -309,8 +317,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (void)mbar_wait(&bars->mma_done, 0);
     }
   } else {
-    // Gradient warps: thread r owns key 128n + r (TMEM lane r).
+    // Gradient warps: thread r owns key 128n + r (TMEM lane r); warpgroup
+    // `half` handles columns [64*half, 64*half + 64).
     const int quad = warp & 3;
+    const int half = warp >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int key = 128 * n + r;
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int bh = b * p.Hq + h;
       // This step's per-row LSE (log2 domain) and Delta in the warp's own
       // buffer (no cross-warp barrier, so an aborting warp cannot strand others).
-      float* lse2 = sScal + (quad * 2 + (s & 1)) * 256;
+      float* lse2 = sScal + (warp * 2 + (s & 1)) * 256;
       float* dlt = lse2 + 128;
       for (int t = lane; t < 128; t += 32) {
         const int row = 128 * m + t;
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Visible rows for this key: row >= key - (Sk - Sq) (causal) and row < Sq.
       const int row_lo = p.causal ? key - (p.Sk - p.Sq) : -0x40000000;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         uint32_t sr[32], dr[32];
         tmem_ld32(tmem + lane_addr + C::kColS + 32 * c, sr);
         tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
@@ -356,8 +366,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
           dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
         }
-        tmem_st16(tmem + lane_addr + C::kColS + 16 * c, pk);
-        tmem_st16(tmem + lane_addr + C::kColDP + 16 * c, dk);
+        const uint32_t pc = 64 * half + 16 * (c - 2 * half);  // own half of the columns
+        tmem_st16(tmem + lane_addr + C::kColS + pc, pk);
+        tmem_st16(tmem + lane_addr + C::kColDP + pc, dk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -369,7 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (nsteps == 0) {
         // No query row sees these keys: their gradients are zero.
         if (key_valid) {
-          for (int c = 0; c < D; c += 4) {
+          for (int c = half * D / 2; c < (half + 1) * D / 2; c += 4) {
             *reinterpret_cast<float4*>(dk_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(dv_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           }
@@ -378,8 +389,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = __all_sync(0xffffffffu, bwd_wait(&bars->acc_full, 0, bars));
         if (ok) {
           tc_fence_after();
-          store_acc_row<D>(tmem + lane_addr + C::kColA0, dk_row, p.scale, key_valid);
-          store_acc_row<D>(tmem + lane_addr + C::kColA1, dv_row, 1.f, key_valid);
+          store_acc_row<D>(tmem + lane_addr + C::kColA0, dk_row, p.scale, key_valid,
+                           half * D / 2, (half + 1) * D / 2);
+          store_acc_row<D>(tmem + lane_addr + C::kColA1, dv_row, 1.f, key_valid,
+                           half * D / 2, (half + 1) * D / 2);
         }
       }
     }
@@ -427,7 +440,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->empty[s], 1);
     }
     mbar_init(&bars->sd_full, 1);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_full, kGradThreads);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -486,8 +499,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (void)mbar_wait(&bars->mma_done, 0);
     }
   } else {
-    // Gradient warps: thread r owns query row 128m + r (TMEM lane r).
+    // Gradient warps: thread r owns query row 128m + r (TMEM lane r); warpgroup
+    // `half` handles keys [64*half, 64*half + 64) of each tile.
     const int quad = warp & 3;
+    const int half = warp >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int row = 128 * m + r;
@@ -501,7 +516,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         uint32_t sr[32], dr[32];
         tmem_ld32(tmem + lane_addr + C::kColS + 32 * c, sr);
         tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
@@ -519,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
         }
-        tmem_st16(tmem + lane_addr + C::kColDP + 16 * c, dk);
+        tmem_st16(tmem + lane_addr + C::kColDP + 64 * half + 16 * (c - 2 * half), dk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -529,13 +544,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float* dq_row = p.out0 + (static_cast<size_t>(bh) * p.Sq + row) * D;
       if (nsteps == 0) {
         if (row_valid)
-          for (int c = 0; c < D; c += 4)
+          for (int c = half * D / 2; c < (half + 1) * D / 2; c += 4)
             *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
         ok = __all_sync(0xffffffffu, bwd_wait(&bars->acc_full, 0, bars));
         if (ok) {
           tc_fence_after();
-          store_acc_row<D>(tmem + lane_addr + C::kColA0, dq_row, p.scale, row_valid);
+          store_acc_row<D>(tmem + lane_addr + C::kColA0, dq_row, p.scale, row_valid,
+                           half * D / 2, (half + 1) * D / 2);
         }
       }
     }
