@@ -407,20 +407,28 @@ def ours_arm(args, rank, world, local_rank, dist_on):
 
 
 def profile_arm(args):
-    """A short run of one kernel for ncu: `--profile prefill|decode`, no flush,
-    no e2e, no CPU baseline; `--batch` shrinks the workload's batch."""
+    """A short run of one path for ncu: `--profile prefill|decode|backward`, no
+    flush, no e2e, no CPU baseline; `--batch` shrinks the workload's batch.
+    `backward` runs one forward, then the Delta, dK/dV and dQ kernels per step."""
     import dataclasses
 
     import tensor_attn_fwd_gb300 as attn
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    w = PREFILL if args.profile == "prefill" else DECODE
+    w = DECODE if args.profile == "decode" else PREFILL
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
     q, k, v = (t.to(device) for t in workload_inputs(w))
     if args.profile == "prefill":
         def fn():
             attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    elif args.profile == "backward":
+        o, lse = attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+        g = torch.Generator().manual_seed(w.seed + 7)
+        dout = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(device)
+
+        def fn():
+            attn.attn_bwd(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale)
     else:
         def fn():
             attn.decode(q, k, v, w.num_splits, w.scale)
@@ -443,7 +451,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
                     help="run a few launches of one kernel (for ncu) and exit")
     ap.add_argument("--batch", type=int, default=0, help="override B in --profile mode")
     args = ap.parse_args()

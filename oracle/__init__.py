@@ -70,6 +70,10 @@ def _load():
                 _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dbl,
                 _vp, _vp, _vp]
             lib.oracle_attn_bwd_f64.restype = ctypes.c_int
+            lib.oracle_attn_bwd_sampled.argtypes = [
+                _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dbl,
+                _vp, _i64, _vp, _i64, _vp, _vp, _vp]
+            lib.oracle_attn_bwd_sampled.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -193,4 +197,30 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float):
                                      _ptr(dv))
     if rc != 0:
         raise ValueError(f"oracle_attn_bwd_f64 failed ({rc})")
+    return dq, dk, dv
+
+
+def attn_bwd_sampled(q, k, v, dout, causal: bool, scale: float, qrows, keys):
+    """Backward at sampled positions on bf16 inputs (any size).
+
+    ``qrows``: flat query-row ids (b*Hq + h)*Sq + i -> dQ [nq, D].
+    ``keys``: flat key ids (b*Hkv + g)*Sk + j -> dK, dV [nk, D] (summed over the
+    group's query heads).  All float64.
+    """
+    B, Hq, Sq, D = (int(s) for s in q.shape)
+    _, Hkv, Sk, _ = (int(s) for s in k.shape)
+    if tuple(dout.shape) != tuple(q.shape) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch")
+    qb, kb, vb, db = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v), _bf16_bits(dout)
+    qrows = np.ascontiguousarray(np.asarray(qrows, dtype=np.int64))
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.int64))
+    dq = np.empty((qrows.size, D))
+    dk = np.empty((keys.size, D))
+    dv = np.empty((keys.size, D))
+    rc = _load().oracle_attn_bwd_sampled(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), B, Hq, Hkv, Sq,
+                                         Sk, D, int(bool(causal)), float(scale), _ptr(qrows),
+                                         qrows.size, _ptr(keys), keys.size, _ptr(dq), _ptr(dk),
+                                         _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd_sampled failed ({rc})")
     return dq, dk, dv

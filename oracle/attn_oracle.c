@@ -396,3 +396,165 @@ int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward at sampled positions, on bf16 inputs, for problems too large for
+ * oracle_attn_bwd_f64.  Same definitions as above:
+ *   dq_out[r]  = dQ of query row qrows[r]   (flat (b*Hq + h)*Sq + i)
+ *   dk_out[t], dv_out[t] = dK, dV of key keys[t]   (flat (b*Hkv + g)*Sk + j)
+ * A key's gradient needs LSE_i and Delta_i of every row i of the group's
+ * heads, so those are computed first for each (b, g) that a sampled key
+ * belongs to (one full row pass each); then each key sums over those rows.
+ * ------------------------------------------------------------------------ */
+
+/* P (normalised), dP and Delta of one query row against its visible keys.
+ * p, dp: scratch of at least Sk doubles.  Returns the number of visible keys. */
+static int64_t bwd_row_bf16(const uint16_t *qr, const uint16_t *dor, const uint16_t *kh,
+                            const uint16_t *vh, int64_t n, int64_t D, double scale,
+                            double *p, double *dp, double *lse_out, double *delta_out)
+{
+    if (n <= 0) {
+        *lse_out = -INFINITY;
+        *delta_out = 0.0;
+        return 0;
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            acc += bf16_to_double(qr[d]) * bf16_to_double(kh[j * D + d]);
+        p[j] = scale * acc;
+    }
+    double m = p[0];
+    for (int64_t j = 1; j < n; ++j)
+        if (p[j] > m) m = p[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        p[j] = exp(p[j] - m);
+        l += p[j];
+    }
+    for (int64_t j = 0; j < n; ++j) p[j] /= l;
+    double delta = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            acc += bf16_to_double(dor[d]) * bf16_to_double(vh[j * D + d]);
+        dp[j] = acc;
+        delta += p[j] * acc;
+    }
+    *lse_out = m + log(l);
+    *delta_out = delta;
+    return n;
+}
+
+int oracle_attn_bwd_sampled(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const uint16_t *dout, int64_t B, int64_t Hq, int64_t Hkv,
+                            int64_t Sq, int64_t Sk, int64_t D, int causal, double scale,
+                            const int64_t *qrows, int64_t nq, const int64_t *keys, int64_t nk,
+                            double *dq_out, double *dk_out, double *dv_out)
+{
+    if (check_dims(B, Hq, Hkv, Sq, Sk, D)) return 1;
+    for (int64_t r = 0; r < nq; ++r)
+        if (qrows[r] < 0 || qrows[r] >= B * Hq * Sq) return 1;
+    for (int64_t t = 0; t < nk; ++t)
+        if (keys[t] < 0 || keys[t] >= B * Hkv * Sk) return 1;
+    int64_t group = Hq / Hkv;
+    int bad = 0;
+
+    /* dQ rows */
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        if (p == NULL || dp == NULL) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < nq; ++r) {
+                int64_t row = qrows[r];
+                int64_t i = row % Sq, bh = row / Sq, h = bh % Hq, b = bh / Hq;
+                int64_t bg = b * Hkv + h / group;
+                const uint16_t *kh = k + bg * Sk * D, *vh = v + bg * Sk * D;
+                double lse, delta;
+                int64_t n = bwd_row_bf16(q + row * D, dout + row * D, kh, vh,
+                                         visible_keys(i, Sq, Sk, causal), D, scale, p, dp,
+                                         &lse, &delta);
+                double *dqr = dq_out + r * D;
+                for (int64_t d = 0; d < D; ++d) dqr[d] = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    double ds = p[j] * (dp[j] - delta);
+                    for (int64_t d = 0; d < D; ++d) dqr[d] += scale * ds * bf16_to_double(kh[j * D + d]);
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    if (bad) return bad;
+
+    /* dK / dV keys, one (b, g) at a time */
+    double *lse_g = (double *)malloc(sizeof(double) * (size_t)(group * Sq > 0 ? group * Sq : 1));
+    double *delta_g = (double *)malloc(sizeof(double) * (size_t)(group * Sq > 0 ? group * Sq : 1));
+    char *done = (char *)calloc((size_t)(nk > 0 ? nk : 1), 1);
+    if (lse_g == NULL || delta_g == NULL || done == NULL) bad = 2;
+    for (int64_t t0 = 0; t0 < nk && !bad; ++t0) {
+        if (done[t0]) continue;
+        int64_t bg = keys[t0] / Sk, b = bg / Hkv, g = bg % Hkv;
+        const uint16_t *kh = k + bg * Sk * D, *vh = v + bg * Sk * D;
+        /* row statistics of the group's heads */
+#pragma omp parallel
+        {
+            double *p = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+            double *dp = (double *)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+            if (p == NULL || dp == NULL) {
+#pragma omp atomic write
+                bad = 2;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (int64_t gr = 0; gr < group * Sq; ++gr) {
+                    int64_t h = g * group + gr / Sq, i = gr % Sq;
+                    int64_t row = (b * Hq + h) * Sq + i;
+                    bwd_row_bf16(q + row * D, dout + row * D, kh, vh,
+                                 visible_keys(i, Sq, Sk, causal), D, scale, p, dp,
+                                 &lse_g[gr], &delta_g[gr]);
+                }
+            }
+            free(p);
+            free(dp);
+        }
+        if (bad) break;
+        /* every sampled key of this (b, g) */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t t = t0; t < nk; ++t) {
+            if (keys[t] / Sk != bg) continue;
+            done[t] = 1;
+            int64_t j = keys[t] % Sk;
+            double *dkr = dk_out + t * D, *dvr = dv_out + t * D;
+            for (int64_t d = 0; d < D; ++d) {
+                dkr[d] = 0.0;
+                dvr[d] = 0.0;
+            }
+            for (int64_t gr = 0; gr < group * Sq; ++gr) {
+                int64_t h = g * group + gr / Sq, i = gr % Sq;
+                if (j >= visible_keys(i, Sq, Sk, causal)) continue;
+                int64_t row = (b * Hq + h) * Sq + i;
+                const uint16_t *qr = q + row * D, *dor = dout + row * D;
+                double s = 0.0, dpv = 0.0;
+                for (int64_t d = 0; d < D; ++d) {
+                    s += bf16_to_double(qr[d]) * bf16_to_double(kh[j * D + d]);
+                    dpv += bf16_to_double(dor[d]) * bf16_to_double(vh[j * D + d]);
+                }
+                double pij = exp(scale * s - lse_g[gr]);
+                double ds = pij * (dpv - delta_g[gr]);
+                for (int64_t d = 0; d < D; ++d) {
+                    dkr[d] += scale * ds * bf16_to_double(qr[d]);
+                    dvr[d] += pij * bf16_to_double(dor[d]);
+                }
+            }
+        }
+    }
+    free(lse_g);
+    free(delta_g);
+    free(done);
+    return bad;
+}

@@ -59,3 +59,37 @@ def test_bwd_heads(Hq, Hkv):
 
 def test_bwd_longer():
     run_bwd_case(1, 4, 1, 1024, 1024, 128, True, seed=99)
+
+
+def test_bwd_full_size_sampled():
+    """Causal GQA B2 Hq32 Hkv8 S8192 D128 (the prefill workload), as the benchmark
+    runs it; dQ on sampled query rows, dK/dV on sampled keys of two KV heads."""
+    from attn_inputs import WORKLOADS, sample_rows, workload_inputs
+    w = WORKLOADS[3]
+    q, k, v = workload_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 7)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    del qd, kd, vd, dod, o, lse
+    rows = sample_rows(w.B, w.Hq, w.Sq, n_random=48, seed=w.seed)
+    pick = torch.randperm(rows.numel(), generator=torch.Generator().manual_seed(5))[:96]
+    rows = rows[pick].sort().values
+    S = w.Sk
+    keys = []
+    for bg in (0 * w.Hkv + 3, 1 * w.Hkv + 6):
+        keys += [bg * S + j for j in (0, 1, 127, 128, 4095, 4096, S - 129, S - 1)]
+    keys = torch.tensor(keys + [bg * S + int(j) for j in
+                                torch.randint(0, S, (8,), generator=torch.Generator().manual_seed(6))])
+    dq_ref, dk_ref, dv_ref = oracle.attn_bwd_sampled(q, k, v, do, w.causal, w.scale,
+                                                     rows.numpy(), keys.numpy())
+    got = {"dq": dq.reshape(-1, w.D)[rows.cuda()], "dk": dk.reshape(-1, w.D)[keys.cuda()],
+           "dv": dv.reshape(-1, w.D)[keys.cuda()]}
+    for name, ref in (("dq", dq_ref), ("dk", dk_ref), ("dv", dv_ref)):
+        g_np = got[name].cpu().double().numpy()
+        assert np.all(np.isfinite(g_np)), name
+        err = float(np.max(np.abs(g_np - ref))) / max(float(np.max(np.abs(ref))), 1.0)
+        assert err <= REL_TOL, f"{name}: relative max error {err:.3e}"

@@ -104,3 +104,19 @@ def test_dv_column_sums_and_zero_query():
     qz = torch.zeros_like(q)
     _, dk, _ = oracle.attn_bwd(qz, k, v, do, True, 0.3)
     np.testing.assert_allclose(dk, 0.0, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Sq,Sk", [(13, 13), (9, 17), (17, 9)])
+def test_sampled_matches_full(causal, Sq, Sk):
+    """The sampled form on bf16 inputs gives the full oracle's values at its rows and keys."""
+    B, Hq, Hkv, D = 2, 6, 2, 8
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Sk, D, seed=40 + Sq + Sk)
+    do = _dout(q.shape, seed=41)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, 0.35)
+    qrows = np.array([0, 5, B * Hq * Sq - 1, Sq + 3, 3 * Sq])
+    keys = np.array([0, Sk - 1, Sk + 2, 3 * Sk + 1, B * Hkv * Sk - 1, 1])
+    sq, sk, sv = oracle.attn_bwd_sampled(q, k, v, do, causal, 0.35, qrows, keys)
+    np.testing.assert_allclose(sq, dq.reshape(-1, D)[qrows], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(sk, dk.reshape(-1, D)[keys], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(sv, dv.reshape(-1, D)[keys], rtol=0, atol=1e-13)
