@@ -122,6 +122,37 @@ ATTN_API int attn_decode_splitkv_varlen(const void *q, const void *k, const void
                                         float scale, void *stream);
 
 /*
+ * Split-KV decode over a paged KV cache (first stage; combine with
+ * attn_combine).  Source: "VDCores: Resource Decoupled Programming and
+ * Execution for Asynchronous GPUs", Evaluation (decode attention whose
+ * per-request length changes step by step); the cache is held in fixed-size
+ * pages so that a sequence can grow without moving its keys.  The pages print
+ * no layout; this one keeps each (page, KV head) block contiguous.
+ *
+ * Key t (0 <= t < seqlens[b]) of sequence b, KV head g, is
+ *   k_cache[block_table[b * max_pages + t / page_size], g, t % page_size, :]
+ * (same for v_cache); sequence b attends to exactly its seqlens[b] keys.
+ *
+ *   q           [B,Hq,1,D] bf16 (as attn_decode_splitkv)
+ *   k_cache, v_cache  [num_pages, Hkv, page_size, D] bf16, 16-byte aligned
+ *   block_table device int32 [B, max_pages]; entries in [0, num_pages).  An
+ *               entry outside that range that a sequence reaches sets
+ *               ATTN_ERR_INVALID_ARG in the device status word
+ *               (attn_debug_status) and that block reads page 0 instead.
+ *   seqlens     device int32 [B], clamped to [0, max_pages * page_size]
+ *   page_size   a multiple of 32 (else ATTN_ERR_UNSUPPORTED)
+ *   o_part, lse_part, num_splits, scale, stream: as attn_decode_splitkv,
+ *   except the split rule: chunk = 32 * ceil(ceil(len / num_splits) / 32)
+ *   (whole 32-key blocks), split s covers [s*chunk, min(len, (s+1)*chunk)).
+ *   1 <= num_splits <= max_pages * page_size.
+ */
+ATTN_API int attn_decode_splitkv_paged(const void *q, const void *k_cache, const void *v_cache,
+                                       const int *block_table, const int *seqlens,
+                                       float *o_part, float *lse_part, int B, int Hq, int Hkv,
+                                       int num_pages, int page_size, int max_pages, int D,
+                                       int num_splits, float scale, void *stream);
+
+/*
  * Split-KV decode, second stage: log-sum-exp combine of the partials.
  * Source: same page (FlashDecoding's reduction across key splits).
  *   lse = ln sum_s exp(lse_s);  o = sum_s exp(lse_s - lse) * o_s

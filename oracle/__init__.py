@@ -59,7 +59,7 @@ def _load():
                 _dbl, _vp, _i64, _vp, _vp]
             lib.oracle_attn_fwd_rows.restype = ctypes.c_int
             lib.oracle_decode_split.argtypes = [
-                _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _dbl, _vp, _vp]
+                _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _dbl, _vp, _vp]
             lib.oracle_decode_split.restype = ctypes.c_int
             lib.oracle_combine.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _vp]
             lib.oracle_combine.restype = ctypes.c_int
@@ -124,8 +124,12 @@ def attn_fwd(q, k, v, causal: bool, scale: float, rows=None):
     return o, lse
 
 
-def decode_split(q, k, v, num_splits: int, scale: float):
-    """Per-split partials: O_s [ns,B,Hq,D] and LSE_s [ns,B,Hq] (float64)."""
+def decode_split(q, k, v, num_splits: int, scale: float, align: int = 1):
+    """Per-split partials: O_s [ns,B,Hq,D] and LSE_s [ns,B,Hq] (float64).
+
+    Split s covers keys [s*c, min(Sk, (s+1)*c)) with c = ceil(Sk/ns) rounded up
+    to a multiple of ``align``.
+    """
     B, Hq, Sq, D = (int(s) for s in q.shape)
     if Sq != 1:
         raise ValueError("decode takes one query row per head")
@@ -135,7 +139,7 @@ def decode_split(q, k, v, num_splits: int, scale: float):
     o = np.empty((ns, B, Hq, D), dtype=np.float64)
     lse = np.empty((ns, B, Hq), dtype=np.float64)
     rc = _load().oracle_decode_split(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Sk, D,
-                                     ns, float(scale), _ptr(o), _ptr(lse))
+                                     ns, int(align), float(scale), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_decode_split failed ({rc})")
     return o, lse
@@ -224,3 +228,23 @@ def attn_bwd_sampled(q, k, v, dout, causal: bool, scale: float, qrows, keys):
     if rc != 0:
         raise ValueError(f"oracle_attn_bwd_sampled failed ({rc})")
     return dq, dk, dv
+
+
+def gather_paged(cache, block_table, seqlens, b: int):
+    """The keys (or values) of sequence ``b`` from a paged cache, in order.
+
+    cache [num_pages, Hkv, page_size, D]; block_table [B, max_pages]; key t of
+    sequence b is cache[block_table[b, t // page_size], :, t % page_size, :].
+    Returns [1, Hkv, seqlens[b], D] with the cache's dtype.  Pure indexing.
+    """
+    import torch
+    cache = cache.detach().to("cpu")
+    table = block_table.detach().to("cpu").to(torch.int64)
+    n = int(seqlens[b])
+    num_pages, Hkv, page, D = cache.shape
+    t = torch.arange(n, dtype=torch.int64)
+    pages = table[b, t // page]
+    if n and (int(pages.min()) < 0 or int(pages.max()) >= num_pages):
+        raise ValueError("block table entry out of range")
+    rows = cache[pages, :, t % page, :]          # [n, Hkv, D]
+    return rows.permute(1, 0, 2).unsqueeze(0).contiguous()

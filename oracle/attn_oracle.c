@@ -169,15 +169,18 @@ int oracle_attn_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
  * Split-KV decode partials (Sq = 1, no mask).
  *   q: [B,Hq,1,D]; k, v: [B,Hkv,Sk,D] (bf16 bits).
  *   o_part: [ns,B,Hq,D]; lse_part: [ns,B,Hq].
+ *   align >= 1: the chunk ceil(Sk/ns) is rounded up to a multiple of align
+ *   (1 = the plain rule; the paged-cache decode splits whole blocks of keys).
  */
 int oracle_decode_split(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         int64_t B, int64_t Hq, int64_t Hkv, int64_t Sk, int64_t D,
-                        int64_t ns, double scale, double *o_part,
+                        int64_t ns, int64_t align, double scale, double *o_part,
                         double *lse_part)
 {
-    if (check_dims(B, Hq, Hkv, 1, Sk, D) || ns <= 0) return 1;
+    if (check_dims(B, Hq, Hkv, 1, Sk, D) || ns <= 0 || align <= 0) return 1;
     int64_t group = Hq / Hkv;
     int64_t chunk = (Sk + ns - 1) / ns;
+    chunk = (chunk + align - 1) / align * align;
     int64_t units = ns * B * Hq;
     int bad = 0;
 

@@ -27,7 +27,7 @@ import threading
 import torch
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
-           "attn_combine", "decode", "attn_bwd",
+           "attn_decode_splitkv_paged", "attn_combine", "decode", "decode_paged", "attn_bwd",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
            "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
@@ -58,6 +58,7 @@ _SIGNATURES = {
                              _flt, _vp], _int),
     "attn_decode_splitkv_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
                                     _int, _flt, _vp], _int),
+    "attn_decode_splitkv_paged": ([_vp] * 7 + [_int] * 8 + [_flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
     "attn_bwd": ([_vp] * 10 + [_int] * 7 + [_flt, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
@@ -257,6 +258,56 @@ def attn_decode_splitkv_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
                                             float(scale), _stream_handle(stream))
     _raise_if(st, "attn_decode_splitkv_varlen")
     return o_part, lse_part
+
+
+def attn_decode_splitkv_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_table: torch.Tensor, seqlens: torch.Tensor, num_splits: int,
+                              scale: float | None = None, o_part: torch.Tensor | None = None,
+                              lse_part: torch.Tensor | None = None, stream=None):
+    """Split-KV decode partials over a paged cache.
+
+    k_cache/v_cache [num_pages,Hkv,page_size,D] bf16; block_table int32 CUDA
+    [B,max_pages]; seqlens int32 CUDA [B].  Key t of sequence b is row
+    t % page_size of page block_table[b, t // page_size].
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k_cache", k_cache, 4)
+    _check_bf16("v_cache", v_cache, 4)
+    B, Hq, Sq, D = q.shape
+    _check(Sq == 1, "decode takes one query row per head (q.shape[2] == 1)")
+    num_pages, Hkv, page_size, Dk = k_cache.shape
+    _check(Dk == D and tuple(v_cache.shape) == tuple(k_cache.shape), "q/cache shape mismatch")
+    for name, t in (("block_table", block_table), ("seqlens", seqlens)):
+        _check(isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32
+               and t.is_contiguous() and t.device == q.device,
+               f"{name} must be a contiguous int32 tensor on q's device")
+    _check(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_pages]")
+    _check(tuple(seqlens.shape) == (B,), "seqlens must be [B]")
+    _check(k_cache.device == q.device and v_cache.device == q.device, "q and caches must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ns = int(num_splits)
+    o_part = _out(o_part, (ns, B, Hq, D), q.device, "o_part")
+    lse_part = _out(lse_part, (ns, B, Hq), q.device, "lse_part")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_decode_splitkv_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           block_table.data_ptr(), seqlens.data_ptr(),
+                                           o_part.data_ptr(), lse_part.data_ptr(), B, Hq, Hkv,
+                                           num_pages, page_size, block_table.shape[1], D, ns,
+                                           float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_decode_splitkv_paged")
+    return o_part, lse_part
+
+
+def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_table: torch.Tensor, seqlens: torch.Tensor, num_splits: int,
+                 scale: float | None = None, workspace=None, o=None, lse=None, stream=None):
+    """Paged split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq])."""
+    o_part, lse_part = (None, None) if workspace is None else workspace
+    o_part, lse_part = attn_decode_splitkv_paged(q, k_cache, v_cache, block_table, seqlens,
+                                                 num_splits, scale, o_part, lse_part, stream)
+    return attn_combine(o_part, lse_part, o, lse, stream)
 
 
 def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor | None = None,

@@ -191,14 +191,15 @@ namespace {
 
 int decode_common(const void* q, const void* k, const void* v, const int* seqlens,
                   float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
-                  int num_splits, float scale, void* stream) {
+                  int num_splits, float scale, void* stream, const PagedKV* paged = nullptr) {
   if (!q || !k || !v || !o_part || !lse_part) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > Sk) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * Hkv * Sk * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
+  if (paged == nullptr && static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
+    return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
   const int head_slices = (Hq / Hkv + 15) / 16;  // query heads per decode CTA: 16
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535)
@@ -211,7 +212,7 @@ int decode_common(const void* q, const void* k, const void* v, const int* seqlen
   if (status == nullptr) return ATTN_ERR_CUDA;
   const cudaError_t e =
       launch_decode_splitkv(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
-                            static_cast<cudaStream_t>(stream), status, seqlens);
+                            static_cast<cudaStream_t>(stream), status, seqlens, paged);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -231,6 +232,31 @@ int attn_decode_splitkv_varlen(const void* q, const void* k, const void* v, cons
   if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
   return decode_common(q, k, v, seqlens, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
                        stream);
+}
+
+int attn_decode_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
+                              const int* block_table, const int* seqlens, float* o_part,
+                              float* lse_part, int B, int Hq, int Hkv, int num_pages,
+                              int page_size, int max_pages, int D, int num_splits, float scale,
+                              void* stream) {
+  if (!block_table || !seqlens) return ATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0 || page_size <= 0 || max_pages <= 0) return ATTN_ERR_INVALID_ARG;
+  if (page_size % 32 != 0) return ATTN_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
+  const long long capacity = static_cast<long long>(max_pages) * page_size;
+  if (capacity > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+  if (Hkv > 0 && static_cast<long long>(num_pages) * Hkv > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
+  if (Hkv > 0 && D > 0 &&
+      static_cast<long long>(num_pages) * Hkv * page_size * D > kMaxElems)
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * max_pages > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+  const PagedKV paged{block_table, page_size, max_pages, num_pages};
+  // The contiguous-size checks of decode_common apply to the capacity; the
+  // cache itself is num_pages pages, checked above.
+  return decode_common(q, k_cache, v_cache, seqlens, o_part, lse_part, B, Hq, Hkv,
+                       static_cast<int>(capacity), D, num_splits, scale, stream, &paged);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,

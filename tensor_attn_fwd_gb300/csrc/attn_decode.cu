@@ -93,9 +93,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
                           const __nv_bfloat16* __restrict__ q, float* __restrict__ o_part,
-                          float* __restrict__ lse_part, const int* __restrict__ seqlens, int B,
-                          int Hq, int Hkv, int Sk, int num_splits, int head_slices,
-                          float scale_log2, int* status) {
+                          float* __restrict__ lse_part, const int* __restrict__ seqlens,
+                          const int* __restrict__ block_table, int page_size, int max_pages,
+                          int num_pages, int B, int Hq, int Hkv, int Sk, int num_splits,
+                          int head_slices, float scale_log2, int* status) {
   using C = DecCfg<D>;
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NT = D / 8;   // n-tiles of O += P V
@@ -120,7 +121,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 
   // This sequence's keys: all Sk, or its own length (clamped to [0, Sk]).
   const int len = seqlens != nullptr ? min(max(__ldg(seqlens + b), 0), Sk) : Sk;
-  const int chunk = (len + num_splits - 1) / num_splits;
+  int chunk = (len + num_splits - 1) / num_splits;
+  // Paged: whole 32-key blocks per split, so no block straddles two pages.
+  if (block_table != nullptr) chunk = (chunk + kBlk - 1) / kBlk * kBlk;
   const long long kb64 = static_cast<long long>(split) * chunk;
   const int key_begin = kb64 < len ? static_cast<int>(kb64) : len;
   const int key_end = min(key_begin + chunk, len);
@@ -144,11 +147,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int key0 = key_begin + (warp + (li >> 1) * kWarps) * kBlk;
     const int slot = li % kSlots;
     uint8_t* dst = my_ring + slot * C::kSlotBytes;
+    int plane = bkv, row = key0;
+    if (block_table != nullptr) {
+      // key0 is a multiple of 32 and page_size of 32: the block is inside one page.
+      const int page = key0 / page_size;
+      int pid = __ldg(block_table + static_cast<size_t>(b) * max_pages + page);
+      if (pid < 0 || pid >= num_pages) {
+        record_status(status, ATTN_ERR_INVALID_ARG);  // bad table entry: read page 0 instead
+        pid = 0;
+      }
+      plane = pid * Hkv + g;
+      row = key0 - page * page_size;
+    }
     mbar_arrive_expect_tx(&my_full[slot], C::kSlotBytes);
 #pragma unroll
     for (int s = 0; s < C::kSub; ++s)
-      tma_load_3d(dst + s * C::kSubBytes, (li & 1) ? &tmV : &tmK, &my_full[slot], s * 64, key0,
-                  bkv);
+      tma_load_3d(dst + s * C::kSubBytes, (li & 1) ? &tmV : &tmK, &my_full[slot], s * 64, row,
+                  plane);
   };
   int issued = 0;
   if (lane == 0) {
@@ -460,14 +475,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 template <int D>
 cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, const int* seqlens,
-                               float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk,
-                               int num_splits, float scale, cudaStream_t stream, int* status) {
+                               const PagedKV* paged, float* o_part, float* lse_part, int B,
+                               int Hq, int Hkv, int Sk, int num_splits, float scale,
+                               cudaStream_t stream, int* status) {
   using C = DecCfg<D>;
   const int G = Hq / Hkv;
   const int head_slices = (G + kRows - 1) / kRows;
+  // Contiguous: planes are (b, kv head) with Sk rows.  Paged: planes are
+  // (page, kv head) with page_size rows.
+  const int rows = paged != nullptr ? paged->page_size : Sk;
+  const int planes = paged != nullptr ? paged->num_pages * Hkv : B * Hkv;
   CUtensorMap tmK, tmV;
-  if (!encode_bf16_map(&tmK, k, D, Sk, B * Hkv, kBlk) ||
-      !encode_bf16_map(&tmV, v, D, Sk, B * Hkv, kBlk))
+  if (!encode_bf16_map(&tmK, k, D, rows, planes, kBlk) ||
+      !encode_bf16_map(&tmV, v, D, rows, planes, kBlk))
     return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(decode_splitkv_kernel<D>),
                                    static_cast<int>(C::kSmemBytes));
@@ -475,8 +495,10 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, cons
   const dim3 grid(num_splits, Hkv * head_slices, B);
   const float scale_log2 = scale * 1.4426950408889634f;
   decode_splitkv_kernel<D><<<grid, kWarps * 32, C::kSmemBytes, stream>>>(
-      tmK, tmV, static_cast<const __nv_bfloat16*>(q), o_part, lse_part, seqlens, B, Hq, Hkv, Sk,
-      num_splits, head_slices, scale_log2, status);
+      tmK, tmV, static_cast<const __nv_bfloat16*>(q), o_part, lse_part, seqlens,
+      paged != nullptr ? paged->block_table : nullptr, paged != nullptr ? paged->page_size : 0,
+      paged != nullptr ? paged->max_pages : 0, paged != nullptr ? paged->num_pages : 0, B, Hq, Hkv,
+      Sk, num_splits, head_slices, scale_log2, status);
   return cudaGetLastError();
 }
 
@@ -485,12 +507,12 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, cons
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
                                   int num_splits, float scale, cudaStream_t stream, int* status,
-                                  const int* seqlens) {
+                                  const int* seqlens, const PagedKV* paged) {
   if (D == 128)
-    return launch_decode_impl<128>(q, k, v, seqlens, o_part, lse_part, B, Hq, Hkv, Sk,
+    return launch_decode_impl<128>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
                                    num_splits, scale, stream, status);
-  return launch_decode_impl<64>(q, k, v, seqlens, o_part, lse_part, B, Hq, Hkv, Sk, num_splits,
-                                scale, stream, status);
+  return launch_decode_impl<64>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
+                                num_splits, scale, stream, status);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,

@@ -33,11 +33,21 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
                             float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                             float scale, cudaStream_t stream, int* status);
 
+// Paged KV cache: k, v are [num_pages, Hkv, page_size, D]; key t of sequence b
+// is row t % page_size of page block_table[b * max_pages + t / page_size].
+struct PagedKV {
+  const int* block_table;  // device int32 [B, max_pages]
+  int page_size;           // a multiple of 32
+  int max_pages;
+  int num_pages;
+};
+
 // seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).
+// paged: optional page layout (then Sk = max_pages * page_size, the capacity).
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
                                   int num_splits, float scale, cudaStream_t stream, int* status,
-                                  const int* seqlens = nullptr);
+                                  const int* seqlens = nullptr, const PagedKV* paged = nullptr);
 
 // Backward: Delta into `delta` ([B,Hq,Sq]), then dK/dV and dQ kernels.
 cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const float* o,

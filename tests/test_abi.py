@@ -77,6 +77,32 @@ def test_decode_varlen_rejects(lib, kw, code):
     assert decv(lib, **kw) == code
 
 
+def decp(lib, q=A, k=A, v=A, bt=A, sl=A, op=A, lp=A, B=1, Hq=4, Hkv=1, num_pages=8, page=64,
+         max_pages=4, D=128, ns=4, scale=0.1):
+    return lib.attn_decode_splitkv_paged(q, k, v, bt, sl, op, lp, B, Hq, Hkv, num_pages, page,
+                                         max_pages, D, ns, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bt=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(sl=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(bt=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(sl=A + 1), attn.ATTN_ERR_MISALIGNED),
+    (dict(page=48), attn.ATTN_ERR_UNSUPPORTED),      # not a multiple of 32
+    (dict(page=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(max_pages=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=257), attn.ATTN_ERR_INVALID_ARG),      # more splits than the capacity
+    (dict(max_pages=1 << 25, page=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(k=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+])
+def test_decode_paged_rejects(lib, kw, code):
+    assert decp(lib, **kw) == code
+
+
 def comb(lib, op=A, lp=A, o=A, lse=A, B=1, Hq=4, D=128, ns=4):
     return lib.attn_combine(op, lp, o, lse, B, Hq, D, ns, None)
 

@@ -250,16 +250,17 @@ def test_row_selection_matches_full():
     np.testing.assert_array_equal(Lr, L.reshape(-1)[rows])
 
 
+@pytest.mark.parametrize("align", [1, 32])
 @pytest.mark.parametrize("Sk", [1, 7, 10, 64, 100])
-def test_split_invariance(Sk):
+def test_split_invariance(Sk, align):
     B, Hq, Hkv, D = 2, 8, 2, 16
     q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=17 + Sk)
     O, L = oracle.attn_fwd(q, k, v, False, 0.25)
     for ns in sorted({1, 2, 3, 8, Sk}):
         if ns > Sk:
             continue
-        op, lp = oracle.decode_split(q, k, v, ns, 0.25)
-        chunk = -(-Sk // ns)
+        op, lp = oracle.decode_split(q, k, v, ns, 0.25, align=align)
+        chunk = -(-(-(-Sk // ns)) // align) * align
         for s in range(ns):  # empty splits carry -inf and zeros
             if s * chunk >= Sk:
                 assert np.all(lp[s] == -np.inf) and np.all(op[s] == 0.0)
@@ -285,3 +286,44 @@ def test_invalid_arguments_rejected():
     q, k, v = make_qkv(1, 3, 2, 4, 4, 8, seed=1)  # Hq % Hkv != 0
     with pytest.raises(ValueError):
         oracle.attn_fwd(q, k, v, False, 1.0)
+
+
+def test_aligned_split_boundaries():
+    """align=32: split s holds exactly keys [32*ceil(ceil(Sk/ns)/32)*s, ...)."""
+    B, Hq, Hkv, Sk, D = 1, 2, 1, 100, 8
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=5)
+    op, lp = oracle.decode_split(q, k, v, 3, 0.5, align=32)   # chunk 34 -> 64
+    o0, l0 = oracle.attn_fwd(q, k[:, :, :64], v[:, :, :64], False, 0.5)
+    o1, l1 = oracle.attn_fwd(q, k[:, :, 64:], v[:, :, 64:], False, 0.5)
+    np.testing.assert_array_equal(op[0], o0[:, :, 0])
+    np.testing.assert_array_equal(lp[0], l0[:, :, 0])
+    np.testing.assert_array_equal(op[1], o1[:, :, 0])
+    np.testing.assert_array_equal(lp[1], l1[:, :, 0])
+    assert np.all(lp[2] == -np.inf) and np.all(op[2] == 0.0)
+
+
+def test_gather_paged_recovers_sequences():
+    """A cache built from contiguous K with shuffled pages gathers back to each
+    sequence's prefix, bit for bit; unused pages (NaN) are never read."""
+    B, Hkv, Sk, D, page = 3, 2, 96, 8, 32
+    _, k, _ = make_qkv(B, Hkv, Hkv, 1, Sk, D, seed=9)
+    npp = Sk // page
+    num_pages = B * npp + 2
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(3))
+    cache = torch.full((num_pages, Hkv, page, D), float("nan")).to(torch.bfloat16)
+    table = torch.zeros((B, npp), dtype=torch.int32)
+    for b in range(B):
+        for p in range(npp):
+            pid = int(perm[b * npp + p])
+            cache[pid] = k[b, :, p * page:(p + 1) * page]
+            table[b, p] = pid
+    lens = torch.tensor([0, 33, 96], dtype=torch.int32)
+    for b in range(B):
+        got = oracle.gather_paged(cache, table, lens, b)
+        n = int(lens[b])
+        assert got.shape == (1, Hkv, n, D)
+        assert torch.equal(got.view(torch.int16), k[b:b + 1, :, :n].contiguous().view(torch.int16))
+    bad = table.clone()
+    bad[1, 1] = num_pages
+    with pytest.raises(ValueError):
+        oracle.gather_paged(cache, bad, lens, 1)
