@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, Hq % Hkv != 0, ... */
-    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. D not in {64, 128}) */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. an unsupported D) */
     ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,         /* the CUDA runtime reported an error */
     ATTN_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (device status) */
@@ -60,7 +60,8 @@ typedef enum {
  *
  *   q  [B,Hq,Sq,D] bf16     k, v [B,Hkv,Sk,D] bf16
  *   o  [B,Hq,Sq,D] fp32     lse  [B,Hq,Sq]    fp32
- *   B >= 1, Hq >= 1, Hkv >= 1, Hq % Hkv == 0, Sq >= 1, Sk >= 1, D in {64, 128}
+ *   B >= 1, Hq >= 1, Hkv >= 1, Hq % Hkv == 0, Sq >= 1, Sk >= 1,
+ *   D in {64, 128, 256} (D = 256 runs a one-query-tile-per-CTA kernel)
  *   causal in {0, 1}; scale is applied to QK^T (callers usually pass 1/sqrt(D)).
  * All pointers must be 16-byte aligned.
  */

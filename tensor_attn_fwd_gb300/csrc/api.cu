@@ -162,9 +162,9 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, int o_bf16,
   if (static_cast<long long>(B) * Hq * Sq * D > kMaxElems ||
       static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
     return ATTN_ERR_UNSUPPORTED;
-  // Work items (B*Hq*ceil(Sq/256)) are indexed with int.
-  if (static_cast<long long>(B) * Hq * ((Sq + 255) / 256) > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // Work items (B*Hq*ceil(Sq/256), or ceil(Sq/128) at D = 256) are indexed with int.
+  if (static_cast<long long>(B) * Hq * ((Sq + 127) / 128) > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_MISALIGNED;
   int* status = status_word_device_ptr();

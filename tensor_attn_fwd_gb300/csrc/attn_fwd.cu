@@ -624,6 +624,9 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, int o_bf16,
                             float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
                             float scale, cudaStream_t stream, int* status) {
+  if (D == 256)
+    return launch_attn_fwd_d256(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+                                stream, status);
   if (D == 128)
     return launch_fwd_impl<128>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
                                 stream, status);

@@ -42,6 +42,12 @@ struct PagedKV {
   int num_pages;
 };
 
+// Head dimension 256 (one query tile per CTA, double-buffered S); called by
+// launch_attn_fwd.
+cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, void* o, int o_bf16,
+                                 float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
+                                 float scale, cudaStream_t stream, int* status);
+
 // seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).
 // paged: optional page layout (then Sk = max_pages * page_size, the capacity).
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,

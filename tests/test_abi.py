@@ -121,7 +121,8 @@ def comb(lib, op=A, lp=A, o=A, lse=A, B=1, Hq=4, D=128, ns=4):
     (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
     (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
-    (dict(D=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=192), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(D=512), attn.ATTN_ERR_UNSUPPORTED),
     (dict(Sq=(1 << 30) + 1), attn.ATTN_ERR_UNSUPPORTED),
     (dict(q=M), attn.ATTN_ERR_MISALIGNED),
     (dict(v=M), attn.ATTN_ERR_MISALIGNED),
