@@ -74,6 +74,10 @@ def _load():
                 _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dbl,
                 _vp, _i64, _vp, _i64, _vp, _vp, _vp]
             lib.oracle_attn_bwd_sampled.restype = ctypes.c_int
+            lib.oracle_qkv_rope.argtypes = [
+                _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _dbl, ctypes.c_int, _vp, _i64,
+                _vp, _vp, _vp]
+            lib.oracle_qkv_rope.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -248,3 +252,33 @@ def gather_paged(cache, block_table, seqlens, b: int):
         raise ValueError("block table entry out of range")
     rows = cache[pages, :, t % page, :]          # [n, Hkv, D]
     return rows.permute(1, 0, 2).unsqueeze(0).contiguous()
+
+
+def qkv_rope(x, w, positions, Hq: int, Hkv: int, D: int, base: float = 10000.0,
+             style: int = 0, tokens=None):
+    """QKV projection of x [T, hidden] by w [(Hq+2Hkv)*D, hidden] (bf16), then
+    RoPE on the Q and K heads at positions [T] (int32).
+
+    style 0 rotates dims (2i, 2i+1), style 1 rotates dims (i, i+D/2).
+    Returns float64 q [n, Hq, D], k [n, Hkv, D], v [n, Hkv, D] for the tokens
+    listed in ``tokens`` (default: all T).
+    """
+    xb, wb = _bf16_bits(x), _bf16_bits(w)
+    T, hidden = xb.shape
+    if wb.shape != ((Hq + 2 * Hkv) * D, hidden):
+        raise ValueError("w must be [(Hq+2*Hkv)*D, hidden]")
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+    if pos.shape != (T,):
+        raise ValueError("positions must be [T]")
+    toks = np.arange(T, dtype=np.int64) if tokens is None else \
+        np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    n = toks.size
+    q = np.empty((n, Hq, D))
+    k = np.empty((n, Hkv, D))
+    v = np.empty((n, Hkv, D))
+    rc = _load().oracle_qkv_rope(_ptr(xb), _ptr(wb), _ptr(pos), T, hidden, Hq, Hkv, D,
+                                 float(base), int(style), _ptr(toks), n, _ptr(q), _ptr(k),
+                                 _ptr(v))
+    if rc != 0:
+        raise ValueError(f"oracle_qkv_rope failed ({rc})")
+    return q, k, v

@@ -561,3 +561,78 @@ int oracle_attn_bwd_sampled(const uint16_t *q, const uint16_t *k, const uint16_t
     free(done);
     return bad;
 }
+
+/* ------------------------------------------------------------------------
+ * QKV projection + rotary position embedding, in front of attention.
+ * Source: "A Thread-Register Decoupled GPU Execution Model for Efficient
+ * Tensor Computation", Background (a linear projection of the hidden states
+ * gives Q, K and V, each a GEMM with its weight; RoPE is applied in many
+ * architectures) and "VDCores: Resource Decoupled Programming and Execution
+ * for Asynchronous GPUs", Evaluation (the QKV-Projection + RoPE fused pattern).
+ * The pages print no RoPE formula; the standard rotary embedding is written
+ * out here:
+ *   y[t][n]   = sum_h x[t][h] * w[n][h]          (w holds the rows of Wq, Wk, Wv)
+ *   columns [0, Hq*D) are Q heads, then Hkv K heads, then Hkv V heads;
+ *   theta_i   = base^(-2i/D),  angle = pos_t * theta_i,  i in [0, D/2)
+ *   style 0 (pairs of adjacent dims):  (a, b) = (y[2i], y[2i+1])
+ *   style 1 (dims i and i + D/2):      (a, b) = (y[i], y[i+D/2])
+ *   a' = a cos(angle) - b sin(angle),   b' = a sin(angle) + b cos(angle)
+ * applied to every Q and K head; V is the plain projection.
+ * Outputs for the listed tokens t (t = b*S + s): q [n, Hq, D], k, v [n, Hkv, D].
+ * ------------------------------------------------------------------------ */
+int oracle_qkv_rope(const uint16_t *x, const uint16_t *w, const int32_t *positions,
+                    int64_t T, int64_t hidden, int64_t Hq, int64_t Hkv, int64_t D,
+                    double base, int style, const int64_t *tokens, int64_t ntok,
+                    double *q, double *k, double *v)
+{
+    if (T < 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || D % 2 != 0) return 1;
+    if (style != 0 && style != 1) return 1;
+    for (int64_t r = 0; r < ntok; ++r)
+        if (tokens[r] < 0 || tokens[r] >= T) return 1;
+    int64_t N = (Hq + 2 * Hkv) * D;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *y = (double *)malloc(sizeof(double) * (size_t)N);
+        double *xr = (double *)malloc(sizeof(double) * (size_t)hidden);
+        if (y == NULL || xr == NULL) {
+#pragma omp atomic write
+            bad = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < ntok; ++r) {
+                int64_t t = tokens[r];
+                for (int64_t h = 0; h < hidden; ++h) xr[h] = bf16_to_double(x[t * hidden + h]);
+                for (int64_t n = 0; n < N; ++n) {
+                    double acc = 0.0;
+                    for (int64_t h = 0; h < hidden; ++h)
+                        acc += xr[h] * bf16_to_double(w[n * hidden + h]);
+                    y[n] = acc;
+                }
+                double pos = (double)positions[t];
+                /* rotate every Q and K head */
+                for (int64_t head = 0; head < Hq + Hkv; ++head) {
+                    double *yh = y + head * D;
+                    for (int64_t i = 0; i < D / 2; ++i) {
+                        double theta = pow(base, -2.0 * (double)i / (double)D);
+                        double ang = pos * theta;
+                        double c = cos(ang), s = sin(ang);
+                        int64_t ia = style == 0 ? 2 * i : i;
+                        int64_t ib = style == 0 ? 2 * i + 1 : i + D / 2;
+                        double a = yh[ia], b = yh[ib];
+                        yh[ia] = a * c - b * s;
+                        yh[ib] = a * s + b * c;
+                    }
+                }
+                for (int64_t n = 0; n < Hq * D; ++n) q[r * Hq * D + n] = y[n];
+                for (int64_t n = 0; n < Hkv * D; ++n) {
+                    k[r * Hkv * D + n] = y[Hq * D + n];
+                    v[r * Hkv * D + n] = y[(Hq + Hkv) * D + n];
+                }
+            }
+        }
+        free(y);
+        free(xr);
+    }
+    return bad;
+}
