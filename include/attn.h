@@ -154,6 +154,46 @@ ATTN_API int attn_decode_splitkv_paged(const void *q, const void *k_cache, const
                                        int num_splits, float scale, void *stream);
 
 /*
+ * Rotary-embedding table for attn_qkv_rope.
+ * Source: "A Thread-Register Decoupled GPU Execution Model for Efficient
+ * Tensor Computation", Background (RoPE around the projections); the standard
+ * rotary frequencies theta_i = base^(-2i/D).
+ *   table [max_pos, D/2, 2] fp32 device, 16-byte aligned:
+ *     table[p][i] = (cos(p * theta_i), sin(p * theta_i)), computed in double
+ *     precision and rounded to fp32.
+ *   D even, base > 1 (10000 in the usual models).
+ */
+ATTN_API int attn_rope_table(float *table, int max_pos, int D, float base, void *stream);
+
+/*
+ * QKV projection with the rotary embedding applied in its epilogue, writing
+ * the attention inputs.  Source: same page, Background (the hidden states are
+ * projected to Q, K and V by GEMMs with the weight matrices) and "VDCores:
+ * Resource Decoupled Programming and Execution for Asynchronous GPUs",
+ * Evaluation (QKV-Projection + RoPE as one fused pattern).
+ *
+ *   x  [B*S, hidden] bf16 (token t = b*S + s), hidden % 8 == 0
+ *   w  [(Hq + 2*Hkv)*D, hidden] bf16: the rows of Wq, then Wk, then Wv
+ *      (the usual [out_features, in_features] weight layout)
+ *   y = x w^T; head n of y (columns [n*D, (n+1)*D)) is query head n for
+ *   n < Hq, then Hkv key heads, then Hkv value heads.
+ *   rope_table from attn_rope_table, at least max_pos rows
+ *   positions device int32 [B*S] (position of each token), or NULL for
+ *      position = s; a position outside [0, max_pos) sets
+ *      ATTN_ERR_INVALID_ARG in the device status word and is clamped.
+ *   style 0 rotates dims (2i, 2i+1) of each Q and K head, style 1 rotates
+ *      dims (i, i + D/2):  (a, b) -> (a cos - b sin, a sin + b cos).
+ *   q [B,Hq,S,D], k, v [B,Hkv,S,D] bf16 outputs (the attn_fwd inputs),
+ *      rounded to nearest even from the fp32 accumulator.
+ *   D in {64, 128, 256}; Hq % Hkv == 0.  All pointers 16-byte aligned
+ *   (positions 4-byte).
+ */
+ATTN_API int attn_qkv_rope(const void *x, const void *w, const float *rope_table,
+                           const int *positions, void *q, void *k, void *v, int B, int S,
+                           int hidden, int Hq, int Hkv, int D, int max_pos, int style,
+                           void *stream);
+
+/*
  * Split-KV decode, second stage: log-sum-exp combine of the partials.
  * Source: same page (FlashDecoding's reduction across key splits).
  *   lse = ln sum_s exp(lse_s);  o = sum_s exp(lse_s - lse) * o_s

@@ -14,7 +14,11 @@ Names follow the C ABI:
     attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits) -> (o_part, lse_part)
     attn_combine(o_part, lse_part)              -> (o, lse)
     decode(q, k, v, num_splits)                 -> (o, lse)   both stages
+    attn_decode_splitkv_paged(q, k_cache, v_cache, block_table, seqlens, num_splits)
+    decode_paged(...)                           -> (o, lse)   both stages, paged cache
     attn_bwd(q, k, v, o, lse, dout, causal, scale) -> (dq, dk, dv)
+    attn_rope_table(max_pos, D, base)           -> (cos, sin) table
+    attn_qkv_rope(x, w, table, Hq, Hkv)         -> (q, k, v) bf16, RoPE applied
 Layouts: Q [B,Hq,Sq,D], K/V [B,Hkv,Sk,D] bf16; O [B,Hq,Sq,D], LSE [B,Hq,Sq] fp32.
 """
 from __future__ import annotations
@@ -28,6 +32,7 @@ import torch
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
            "attn_decode_splitkv_paged", "attn_combine", "decode", "decode_paged", "attn_bwd",
+           "attn_rope_table", "attn_qkv_rope",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
            "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
@@ -60,6 +65,8 @@ _SIGNATURES = {
                                     _int, _flt, _vp], _int),
     "attn_decode_splitkv_paged": ([_vp] * 7 + [_int] * 8 + [_flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
+    "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
+    "attn_qkv_rope": ([_vp] * 7 + [_int] * 8 + [_vp], _int),
     "attn_bwd": ([_vp] * 10 + [_int] * 7 + [_flt, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
     "attn_debug_status": ([_vp], _int),
@@ -130,6 +137,16 @@ def _out(t, shape, device, name):
         return torch.empty(shape, dtype=torch.float32, device=device)
     _check(t.is_cuda and t.dtype == torch.float32 and t.is_contiguous(),
            f"{name} must be a contiguous float32 CUDA tensor")
+    _check(tuple(t.shape) == tuple(shape), f"{name} must have shape {tuple(shape)}")
+    _check(t.device == device, f"{name} must be on {device}")
+    return t
+
+
+def _out_bf16(t, shape, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    _check(t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous(),
+           f"{name} must be a contiguous bf16 CUDA tensor")
     _check(tuple(t.shape) == tuple(shape), f"{name} must have shape {tuple(shape)}")
     _check(t.device == device, f"{name} must be on {device}")
     return t
@@ -308,6 +325,62 @@ def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     o_part, lse_part = attn_decode_splitkv_paged(q, k_cache, v_cache, block_table, seqlens,
                                                  num_splits, scale, o_part, lse_part, stream)
     return attn_combine(o_part, lse_part, o, lse, stream)
+
+
+def attn_rope_table(max_pos: int, D: int, base: float = 10000.0, device=None,
+                    out: torch.Tensor | None = None, stream=None):
+    """(cos, sin) table [max_pos, D/2, 2] fp32 of pos * base^(-2i/D), built on the GPU."""
+    if out is None:
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        out = torch.empty((int(max_pos), int(D) // 2, 2), dtype=torch.float32, device=dev)
+    _check(out.is_cuda and out.dtype == torch.float32 and out.is_contiguous()
+           and tuple(out.shape) == (int(max_pos), int(D) // 2, 2),
+           "out must be a contiguous float32 CUDA tensor [max_pos, D/2, 2]")
+    lib = load_library()
+    with torch.cuda.device(out.device):
+        st = lib.attn_rope_table(out.data_ptr(), int(max_pos), int(D), float(base),
+                                 _stream_handle(stream))
+    _raise_if(st, "attn_rope_table")
+    return out
+
+
+def attn_qkv_rope(x: torch.Tensor, w: torch.Tensor, rope_table: torch.Tensor, Hq: int, Hkv: int,
+                  positions: torch.Tensor | None = None, style: int = 0,
+                  q: torch.Tensor | None = None, k: torch.Tensor | None = None,
+                  v: torch.Tensor | None = None, stream=None):
+    """Q, K, V = RoPE(x w^T) split into heads, in the [B, H, S, D] layout of attn_fwd.
+
+    x [B, S, hidden] bf16; w [(Hq+2*Hkv)*D, hidden] bf16 (rows of Wq, Wk, Wv);
+    rope_table from attn_rope_table ([max_pos, D/2, 2]); positions int32 [B, S]
+    (default: s).  style 0 rotates dims (2i, 2i+1), style 1 dims (i, i+D/2).
+    Returns bf16 q [B,Hq,S,D], k [B,Hkv,S,D], v [B,Hkv,S,D].
+    """
+    _check_bf16("x", x, 3)
+    _check(isinstance(w, torch.Tensor) and w.is_cuda and w.dtype == torch.bfloat16
+           and w.is_contiguous() and w.dim() == 2, "w must be a contiguous 2-D bf16 CUDA tensor")
+    B, S, hidden = x.shape
+    max_pos, half, two = rope_table.shape
+    D = 2 * half
+    _check(two == 2 and rope_table.dtype == torch.float32 and rope_table.is_contiguous()
+           and rope_table.device == x.device, "rope_table must come from attn_rope_table")
+    _check(tuple(w.shape) == ((Hq + 2 * Hkv) * D, hidden), "w must be [(Hq+2*Hkv)*D, hidden]")
+    _check(w.device == x.device, "x and w must share a device")
+    pos_ptr = 0
+    if positions is not None:
+        _check(positions.is_cuda and positions.dtype == torch.int32 and positions.is_contiguous()
+               and positions.numel() == B * S and positions.device == x.device,
+               "positions must be a contiguous int32 CUDA tensor with B*S entries")
+        pos_ptr = positions.data_ptr()
+    q = _out_bf16(q, (B, Hq, S, D), x.device, "q")
+    k = _out_bf16(k, (B, Hkv, S, D), x.device, "k")
+    v = _out_bf16(v, (B, Hkv, S, D), x.device, "v")
+    lib = load_library()
+    with torch.cuda.device(x.device):
+        st = lib.attn_qkv_rope(x.data_ptr(), w.data_ptr(), rope_table.data_ptr(), pos_ptr or None,
+                               q.data_ptr(), k.data_ptr(), v.data_ptr(), B, S, hidden, Hq, Hkv,
+                               D, max_pos, int(style), _stream_handle(stream))
+    _raise_if(st, "attn_qkv_rope")
+    return q, k, v
 
 
 def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor | None = None,

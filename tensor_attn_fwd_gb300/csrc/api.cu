@@ -288,6 +288,45 @@ int attn_bwd(const void* q, const void* k, const void* v, const float* o, const 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int attn_rope_table(float* table, int max_pos, int D, float base, void* stream) {
+  if (!table) return ATTN_ERR_INVALID_ARG;
+  if (max_pos <= 0 || D <= 0 || D % 2 != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(base > 1.f) || !std::isfinite(base)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(max_pos) * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(table)) return ATTN_ERR_MISALIGNED;
+  const cudaError_t e = launch_rope_table(table, max_pos, D, static_cast<double>(base),
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_qkv_rope(const void* x, const void* w, const float* rope_table, const int* positions,
+                  void* q, void* k, void* v, int B, int S, int hidden, int Hq, int Hkv, int D,
+                  int max_pos, int style, void* stream) {
+  if (!x || !w || !rope_table || !q || !k || !v) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_pos <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (style != 0 && style != 1) return ATTN_ERR_INVALID_ARG;
+  if (positions == nullptr && max_pos < S) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
+  if (hidden % 8 != 0) return ATTN_ERR_UNSUPPORTED;  // TMA row pitch: a multiple of 16 bytes
+  const long long T = static_cast<long long>(B) * S;
+  const long long N = static_cast<long long>(Hq + 2ll * Hkv) * D;
+  if (T > (1ll << 30) || N > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
+  if (T * hidden > kMaxElems || N * hidden > kMaxElems || T * N > kMaxElems)
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(rope_table) || !aligned16(q) ||
+      !aligned16(k) || !aligned16(v))
+    return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(positions) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const cudaError_t e = launch_qkv_rope(x, w, rope_table, positions, q, k, v, B, S, hidden, Hq,
+                                        Hkv, D, max_pos, style,
+                                        static_cast<cudaStream_t>(stream), status);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_combine(const float* o_part, const float* lse_part, float* o, float* lse, int B, int Hq,
                  int D, int num_splits, void* stream) {
   if (!o_part || !lse_part || !o || !lse) return ATTN_ERR_INVALID_ARG;

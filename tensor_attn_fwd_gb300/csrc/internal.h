@@ -48,6 +48,12 @@ cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, vo
                                  float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
                                  float scale, cudaStream_t stream, int* status);
 
+// QKV projection + rotary embedding (qkv_rope.cu).
+cudaError_t launch_rope_table(float* table, int max_pos, int D, double base, cudaStream_t stream);
+cudaError_t launch_qkv_rope(const void* x, const void* w, const float* rope, const int* positions,
+                            void* q, void* k, void* v, int B, int S, int hidden, int Hq, int Hkv,
+                            int D, int max_pos, int style, cudaStream_t stream, int* status);
+
 // seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).
 // paged: optional page layout (then Sk = max_pages * page_size, the capacity).
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,

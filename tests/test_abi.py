@@ -170,3 +170,37 @@ def test_binding_has_no_fallback_import():
     # The product binding must not reach the oracle.
     src = open(os.path.join(ROOT, "tensor_attn_fwd_gb300", "__init__.py")).read()
     assert "oracle" not in src.replace("no CPU or PyTorch fallback", "")
+
+
+def qkv(lib, x=A, w=A, t=A, pos=A, q=A, k=A, v=A, B=1, S=16, hidden=64, Hq=2, Hkv=1, D=64,
+        max_pos=16, style=0):
+    return lib.attn_qkv_rope(x, w, t, pos, q, k, v, B, S, hidden, Hq, Hkv, D, max_pos, style, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(t=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(S=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(style=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(pos=None, max_pos=8), attn.ATTN_ERR_INVALID_ARG),   # positions s need max_pos >= S
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(hidden=60), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(w=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(pos=A + 2), attn.ATTN_ERR_MISALIGNED),
+])
+def test_qkv_rope_rejects(lib, kw, code):
+    assert qkv(lib, **kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 64, 10000.0), attn.ATTN_ERR_INVALID_ARG),
+    ((A, 0, 64, 10000.0), attn.ATTN_ERR_INVALID_ARG),
+    ((A, 16, 63, 10000.0), attn.ATTN_ERR_INVALID_ARG),
+    ((A, 16, 64, 1.0), attn.ATTN_ERR_INVALID_ARG),
+    ((A, 16, 64, float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    ((M, 16, 64, 10000.0), attn.ATTN_ERR_MISALIGNED),
+])
+def test_rope_table_rejects(lib, args, code):
+    assert lib.attn_rope_table(*args, None) == code
