@@ -8,8 +8,12 @@ workload B=2, Hq=32, Hkv=8, S=8192, D=128; a step is one attn_fwd launch with
 its inputs resident in HBM.  L2 is flushed between steps by writing a 256 MiB
 buffer outside the timed events.  The ``decode`` object reports the split-KV
 decode + combine (B=64, Hq=32, Hkv=8, Sk=4096, D=128, 8 splits) in GB/s of
-algorithmic bytes.  ``e2e`` repeats the prefill through the public API with
-pinned host buffers, the host<->device copies inside the timed region.
+algorithmic bytes.  ``backward`` times attn_bwd on the prefill workload
+(TFLOP/s at 2.5x the forward's FLOPs) and ``qkv_rope`` the fused QKV
+projection + RoPE that produces that workload's Q, K, V from hidden states of
+width 4096 (TFLOP/s at 2*T*hidden*N).  ``e2e`` repeats the prefill through the
+public API with pinned host buffers, the host<->device copies inside the timed
+region.
 
 --impl reference times the fp64 CPU oracle on the same workload (a bounded
 sample of query rows per step) and prints the same line with impl=reference.
@@ -347,6 +351,36 @@ def ours_arm(args, rank, world, local_rank, dist_on):
                     "gpu_launches_per_step": 3}
         del dq, dk, dv, dws, dout
 
+    # ---------------- QKV projection + RoPE producing this workload's Q, K, V
+    qkv_rope = None
+    if not args.no_qkv_rope:
+        hidden = 4096  # Llama-family model width for 32 query heads of 128
+        g = torch.Generator().manual_seed(w.seed + 11)
+        xq = torch.randn((w.B, w.Sq, hidden), generator=g).to(torch.bfloat16).to(device)
+        wq = (torch.randn(((w.Hq + 2 * w.Hkv) * w.D, hidden), generator=g)
+              / math.sqrt(hidden)).to(torch.bfloat16).to(device)
+        table = attn.attn_rope_table(w.Sq, w.D, 10000.0)
+        qo = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
+        ko = torch.empty(k.shape, dtype=torch.bfloat16, device=device)
+        vo = torch.empty(v.shape, dtype=torch.bfloat16, device=device)
+
+        def qkv():
+            attn.attn_qkv_rope(xq, wq, table, w.Hq, w.Hkv, q=qo, k=ko, v=vo, stream=stream)
+
+        r_steps = max(3, min(args.steps, 50))
+        r_times = time_launches(qkv, r_steps, 3, flush_buf, stream)
+        r_ms = sum(r_times) / len(r_times)
+        r_flops = 2.0 * w.B * w.Sq * hidden * (w.Hq + 2 * w.Hkv) * w.D
+        qkv_rope = {"workload": f"x [{w.B},{w.Sq},{hidden}] bf16 -> RoPE(x W^T) as Q,K,V of "
+                                f"{w.name}",
+                    "metric": "QKV projection + RoPE TFLOP/s (2*T*hidden*N)",
+                    "value": r_flops / (r_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": r_ms, "steps": r_steps,
+                    "frac_of_measured_bf16_peak": r_flops / (r_ms * 1e-3) / 1e12
+                    / peaks["bf16_tflops"],
+                    "gpu_launches_per_step": 1}
+        del xq, wq, table, qo, ko, vo
+
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.no_e2e:
@@ -398,6 +432,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
                      "peak_source": f"{peaks_src} cuBLAS bf16 burst"},
         "decode": decode,
         "backward": backward,
+        "qkv_rope": qkv_rope,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": args.steps,
@@ -407,7 +442,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
 
 
 def profile_arm(args):
-    """A short run of one path for ncu: `--profile prefill|decode|backward`, no
+    """A short run of one path for ncu: `--profile prefill|decode|backward|qkv`, no
     flush, no e2e, no CPU baseline; `--batch` shrinks the workload's batch.
     `backward` runs one forward, then the Delta, dK/dV and dQ kernels per step."""
     import dataclasses
@@ -422,6 +457,17 @@ def profile_arm(args):
     if args.profile == "prefill":
         def fn():
             attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    elif args.profile == "qkv":
+        import math as _m
+        hidden = 4096
+        g = torch.Generator().manual_seed(w.seed + 11)
+        xq = torch.randn((w.B, w.Sq, hidden), generator=g).to(torch.bfloat16).to(device)
+        wq = (torch.randn(((w.Hq + 2 * w.Hkv) * w.D, hidden), generator=g)
+              / _m.sqrt(hidden)).to(torch.bfloat16).to(device)
+        table = attn.attn_rope_table(w.Sq, w.D, 10000.0)
+
+        def fn():
+            attn.attn_qkv_rope(xq, wq, table, w.Hq, w.Hkv)
     elif args.profile == "backward":
         o, lse = attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
         g = torch.Generator().manual_seed(w.seed + 7)
@@ -450,8 +496,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-qkv-rope", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward", "qkv"], default=None,
                     help="run a few launches of one kernel (for ncu) and exit")
     ap.add_argument("--batch", type=int, default=0, help="override B in --profile mode")
     args = ap.parse_args()
