@@ -17,9 +17,16 @@
 //                 the gradient warps (one thread per key) turn them into P^T
 //                 and dS^T (bf16, written back into TMEM over S^T / dP^T); then
 //                 dV += P^T dO and dK += dS^T Q accumulate in TMEM.  No atomics.
+//                 Per step the MMA warp issues dV(s) as soon as P^T(s) is in
+//                 TMEM, dK(s) once dS^T(s) is, then S^T(s+1) and dP^T(s+1): the
+//                 gradient warps' exponentials for step s+1 overlap dP^T(s+1),
+//                 and their dS^T overlaps dV, so the tensor core stays busy.
 //   dQ kernel     one CTA per 128-row query tile: S = Q K^T and dP = dO V^T
 //                 recomputed for each visible KV tile, dS written into TMEM,
-//                 dQ += dS K accumulated in TMEM.
+//                 dQ += dS K accumulated in TMEM.  S(s+1) is issued as soon as
+//                 the gradient warps have read S(s), so it overlaps their work
+//                 on step s; K and V stream through separate rings (K is
+//                 needed until dQ(s), V only until dP(s)).
 // Roles (320 threads): warps 0-7 gradient math (two warpgroups, each owning 64
 // of a tile's 128 columns: the backward needs no row reductions, so the split
 // is free), warp 8 MMA issue, warp 9 TMA.  Each warpgroup writes its bf16
@@ -50,16 +57,23 @@ constexpr int kStages = 2;
 constexpr uint32_t kSub = 128 * 128;  // [128 rows x 64 bf16] 128B-swizzled sub-tile
 constexpr float kLog2e = 1.4426950408889634f;
 
+constexpr int kKStages = 3;  // dQ kernel: K ring
+constexpr int kVStages = 2;  // dQ kernel: V ring
+
 template <int D>
 struct BwdCfg {
   static constexpr uint32_t kTile = (D / 64) * kSub;  // one 128 x D bf16 tile
-  // smem: two fixed tiles, kStages x (two streamed tiles), then scalars/barriers
+  // dK/dV smem: two fixed tiles, kStages x (two streamed tiles), then scalars/barriers
   static constexpr uint32_t kFixed = 2 * kTile;
   static constexpr uint32_t kRing = kStages * 2 * kTile;
-  // Per gradient warp, two buffers of (LSE2[128], Delta[128]) for the current step.
-  static constexpr uint32_t kScalars = 8 * 2 * 2 * 128 * 4;
+  // Per gradient warp: -LSE2 and -Delta of its 64 columns for the current step.
+  static constexpr uint32_t kScalars = 8 * 2 * 64 * 4;
   static constexpr uint32_t kBarBytes = 256;
   static constexpr size_t kSmem = 1024 + kFixed + kRing + kScalars + kBarBytes;
+  // dQ smem: Q and dO fixed, a K ring and a V ring, barriers.
+  static constexpr size_t kSmemDq =
+      1024 + kFixed + size_t(kKStages + kVStages) * kTile + kBarBytes;
+  static_assert(kSmem <= 232448 && kSmemDq <= 232448, "shared memory per CTA");
   static constexpr uint32_t kColS = 0, kColDP = 128, kColA0 = 256, kColA1 = 256 + D;
   static constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, false, true);
@@ -67,14 +81,18 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t fixed_full;
-  uint64_t full[kStages], empty[kStages];
-  uint64_t sd_full;   // S and dP of the current step are in TMEM
-  uint64_t p_full;    // P / dS of the current step are in TMEM
+  uint64_t full[kKStages], empty[kKStages];     // dK/dV: Q+dO stages; dQ: K stages
+  uint64_t full_v[kVStages], empty_v[kVStages];  // dQ: V stages
+  uint64_t s_full;    // S (or S^T) of the current step is in TMEM
+  uint64_t dp_full;   // dP (or dP^T) of the current step is in TMEM
+  uint64_t p_ready;   // dK/dV: P^T written; dQ: S read (its columns are free)
+  uint64_t ds_full;   // dS (or dS^T) written
   uint64_t acc_full;  // all accumulating MMAs have completed
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(BwdBars) <= 256, "barrier block too large");
 
 struct BwdParams {
   const float* lse;    // [B,Hq,Sq] natural log
@@ -153,29 +171,25 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
   for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * kSub, map, bar, s * 64, row0, plane);
 }
 
-// Two 128x128 SS products into TMEM: d0 = a0 b0^T, d1 = a1 b1^T (K-major tiles).
+// One 128x128 SS product into TMEM column d_col: a b^T (K-major tiles, D deep).
 template <int D>
-__device__ __forceinline__ void mma_two_ss(uint32_t tmem, uint32_t a0, uint32_t b0, uint32_t a1,
-                                           uint32_t b1) {
+__device__ __forceinline__ void mma_ss_tile(uint32_t tmem, uint32_t d_col, uint32_t a_smem,
+                                            uint32_t b_smem) {
   using C = BwdCfg<D>;
   constexpr uint64_t kDesc = sdesc_sw128(0, 16, 1024);
   constexpr uint32_t kHi = static_cast<uint32_t>(kDesc >> 32);
   constexpr uint32_t kLo = static_cast<uint32_t>(kDesc);
+  const uint32_t a = kLo + (a_smem >> 4);
+  const uint32_t b = kLo + (b_smem >> 4);
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const uint32_t a = kLo + ((which ? a1 : a0) >> 4);
-    const uint32_t b = kLo + ((which ? b1 : b0) >> 4);
-    const uint32_t d = tmem + (which ? C::kColDP : C::kColS);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = ((kk >> 2) * kSub + (kk & 3) * 32) >> 4;
-      const uint64_t ad = desc_from_words(a + off, kHi);
-      const uint64_t bd = desc_from_words(b + off, kHi);
-      if (kk == 0)
-        mma_ss_c<0>(d, ad, bd, C::kIdescSS);
-      else
-        mma_ss_c<1>(d, ad, bd, C::kIdescSS);
-    }
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kSub + (kk & 3) * 32) >> 4;
+    const uint64_t ad = desc_from_words(a + off, kHi);
+    const uint64_t bd = desc_from_words(b + off, kHi);
+    if (kk == 0)
+      mma_ss_c<0>(tmem + d_col, ad, bd, C::kIdescSS);
+    else
+      mma_ss_c<1>(tmem + d_col, ad, bd, C::kIdescSS);
   }
 }
 
@@ -254,8 +268,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->sd_full, 1);
-    mbar_init(&bars->p_full, kGradThreads);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, kGradThreads);
+    mbar_init(&bars->ds_full, kGradThreads);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -296,20 +312,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0 && nsteps > 0) {
       ok = bwd_wait(&bars->fixed_full, 0, bars);
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      // S^T = K Q^T and dP^T = V dO^T of step s (its Q/dO stage must have landed).
+      auto issue_sd = [&](int s) -> bool {
+        const int st = s % kStages;
+        if (!bwd_wait(&bars->full[st], (s / kStages) & 1, bars)) return false;
+        const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
+        mma_ss_tile<D>(tmem, C::kColS, k_addr, q_addr);
+        tc_commit(&bars->s_full);
+        mma_ss_tile<D>(tmem, C::kColDP, v_addr, q_addr + C::kTile);
+        tc_commit(&bars->dp_full);
+        return true;
+      };
+      if (ok) ok = issue_sd(0);
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % kStages;
-        if (!(ok = bwd_wait(&bars->full[st], (s / kStages) & 1, bars))) break;
         const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
         const uint32_t do_addr = q_addr + C::kTile;
-        // S^T = K Q^T and dP^T = V dO^T
-        mma_two_ss<D>(tmem, k_addr, q_addr, v_addr, do_addr);
-        tc_commit(&bars->sd_full);
-        if (!(ok = bwd_wait(&bars->p_full, s & 1, bars))) break;
+        // dV += P^T dO as soon as P^T is in TMEM (B operands MN-major: their
+        // rows are the K dimension) ...
+        if (!(ok = bwd_wait(&bars->p_ready, s & 1, bars))) break;
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q (B operands MN-major: rows are the K dim)
         mma_ts_acc<D>(tmem, C::kColA1, C::kColS, do_addr, s == 0);
+        // ... dK += dS^T Q once dS^T is; then the stage is free.
+        if (!(ok = bwd_wait(&bars->ds_full, s & 1, bars))) break;
+        tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, q_addr, s == 0);
         tc_commit(&bars->empty[st]);
+        // The next step's S^T / dP^T overwrite P^T / dS^T only after the two
+        // products above have read them (same-thread tcgen05 order).
+        if (s + 1 < nsteps && !(ok = issue_sd(s + 1))) break;
       }
       if (ok) tc_commit(&bars->acc_full);
       if (!ok) bwd_record(p.status);
@@ -329,50 +360,98 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int h = g * group + s / per_head;
       const int m = m0 + s % per_head;
       const int bh = b * p.Hq + h;
-      // This step's per-row LSE (log2 domain) and Delta in the warp's own
-      // buffer (no cross-warp barrier, so an aborting warp cannot strand others).
-      float* lse2 = sScal + (warp * 2 + (s & 1)) * 256;
-      float* dlt = lse2 + 128;
-      for (int t = lane; t < 128; t += 32) {
+      // This step's -LSE (log2 domain) and -Delta for the warpgroup's 64
+      // columns, in the warp's own buffer (no cross-warp barrier, so an
+      // aborting warp cannot strand others); read back as broadcast float4.
+      float* nl2 = sScal + warp * 128;
+      float* ndl = nl2 + 64;
+      __syncwarp();  // every lane is done with the previous step's values
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = 64 * half + 32 * u + lane;
         const int row = 128 * m + t;
         const bool rv = row < p.Sq;
-        lse2[t] = rv ? __ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e : 0.f;
-        dlt[t] = rv ? __ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
+        nl2[32 * u + lane] =
+            rv ? -__ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e : 0.f;
+        ndl[32 * u + lane] = rv ? -__ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
       }
       __syncwarp();
-      ok = __all_sync(0xffffffffu, bwd_wait(&bars->sd_full, s & 1, bars));
+      // Visible columns (query rows 128m + col) of this key: [c_lo, c_hi) --
+      // row >= key - (Sk - Sq) under the causal mask, row < Sq.
+      const int row_lo = p.causal ? key - (p.Sk - p.Sq) : -0x40000000;
+      const int c_lo = max(row_lo - 128 * m, 0);
+      const int c_hi = key_valid ? min(p.Sq - 128 * m, 128) : 0;
+      const bool need_mask = __any_sync(0xffffffffu, c_lo > 64 * half || c_hi < 64 * half + 64);
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->s_full, s & 1, bars));
       if (!ok) break;
       tc_fence_after();
-      // Visible rows for this key: row >= key - (Sk - Sq) (causal) and row < Sq.
-      const int row_lo = p.causal ? key - (p.Sk - p.Sq) : -0x40000000;
-#pragma unroll 1
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
-        uint32_t sr[32], dr[32];
+      // P^T for this warpgroup's 64 columns: kept in registers for dS^T and
+      // written (bf16) into its own half of the S^T columns.
+      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+      float pv[64];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        uint32_t sr[32];
         tmem_ld32(tmem + lane_addr + C::kColS + 32 * c, sr);
-        tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(nl2 + 32 * cc + e);
+          float x[4];
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2,
+                           f2_pack(nl.x, nl.y)),
+                    x[0], x[1]);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), sl2,
+                           f2_pack(nl.z, nl.w)),
+                    x[2], x[3]);
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 32 * c + e + u;
-            const int row = 128 * m + col;
-            const bool vis = key_valid && row < p.Sq && row >= row_lo;
-            const float x = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -lse2[col]);
-            pv[u] = vis ? ex2(x) : 0.f;
-            dv[u] = pv[u] * (__uint_as_float(dr[e + u]) - dlt[col]);
+          for (int u = 0; u < 4; ++u) {
+            float pu = ex2(x[u]);
+            if (need_mask) {
+              const int col = 32 * c + e + u;
+              pu = (col >= c_lo && col < c_hi) ? pu : 0.f;
+            }
+            pv[32 * cc + e + u] = pu;
           }
-          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+          pk[e >> 1] = pack_bf16x2(pv[32 * cc + e], pv[32 * cc + e + 1]);
+          pk[(e >> 1) + 1] = pack_bf16x2(pv[32 * cc + e + 2], pv[32 * cc + e + 3]);
         }
-        const uint32_t pc = 64 * half + 16 * (c - 2 * half);  // own half of the columns
-        tmem_st16(tmem + lane_addr + C::kColS + pc, pk);
-        tmem_st16(tmem + lane_addr + C::kColDP + pc, dk);
+        tmem_st16(tmem + lane_addr + C::kColS + 64 * half + 16 * cc, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->p_ready);
+      // dS^T = P^T (dP^T - Delta), into this warpgroup's half of the dP^T columns.
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->dp_full, s & 1, bars));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        uint32_t dr[32];
+        tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nd = *reinterpret_cast<const float4*>(ndl + 32 * cc + e);
+          float d[4];
+          f2_unpack(f2_mul(f2_pack(pv[32 * cc + e], pv[32 * cc + e + 1]),
+                           f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                  f2_pack(nd.x, nd.y))),
+                    d[0], d[1]);
+          f2_unpack(f2_mul(f2_pack(pv[32 * cc + e + 2], pv[32 * cc + e + 3]),
+                           f2_add(f2_pack(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                  f2_pack(nd.z, nd.w))),
+                    d[2], d[3]);
+          dk[e >> 1] = pack_bf16x2(d[0], d[1]);
+          dk[(e >> 1) + 1] = pack_bf16x2(d[2], d[3]);
+        }
+        tmem_st16(tmem + lane_addr + C::kColDP + 64 * half + 16 * cc, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
     }
     if (ok) {
       float* dk_row = p.out0 + (static_cast<size_t>(bg) * p.Sk + key) * D;
@@ -420,8 +499,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + C::kTile;
-  uint8_t* sRing = smem + C::kFixed;  // stage st: K at +0, V at +kTile
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kFixed + C::kRing + C::kScalars);
+  uint8_t* sK = smem + C::kFixed;                // K ring: kKStages tiles
+  uint8_t* sV = sK + kKStages * C::kTile;        // V ring: kVStages tiles
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sV + kVStages * C::kTile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Work: query tile m of head (b, h); CTAs are numbered m-major, highest m
@@ -435,12 +515,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->fixed_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->sd_full, 1);
-    mbar_init(&bars->p_full, kGradThreads);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->full_v[s], 1);
+      mbar_init(&bars->empty_v[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, kGradThreads);
+    mbar_init(&bars->ds_full, kGradThreads);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -461,37 +547,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
       load_tile<D>(sQ, &tmQ, &bars->fixed_full, 128 * m, bh);
       load_tile<D>(sDO, &tmDO, &bars->fixed_full, 128 * m, bh);
+      // K(s) and V(s) in use order; K(s) is held until dQ(s), V(s) until dP(s).
       for (int s = 0; s < nsteps && ok; ++s) {
-        const int st = s % kStages;
-        if (s >= kStages && !(ok = bwd_wait(&bars->empty[st], ((s / kStages) - 1) & 1, bars)))
+        const int sk = s % kKStages, sv = s % kVStages;
+        if (s >= kKStages &&
+            !(ok = bwd_wait(&bars->empty[sk], ((s / kKStages) - 1) & 1, bars)))
           break;
-        uint8_t* dst = sRing + st * 2 * C::kTile;
-        mbar_arrive_expect_tx(&bars->full[st], 2 * C::kTile);
-        load_tile<D>(dst, &tmK, &bars->full[st], 128 * s, bkv);
-        load_tile<D>(dst + C::kTile, &tmV, &bars->full[st], 128 * s, bkv);
+        mbar_arrive_expect_tx(&bars->full[sk], C::kTile);
+        load_tile<D>(sK + sk * C::kTile, &tmK, &bars->full[sk], 128 * s, bkv);
+        if (s >= kVStages &&
+            !(ok = bwd_wait(&bars->empty_v[sv], ((s / kVStages) - 1) & 1, bars)))
+          break;
+        mbar_arrive_expect_tx(&bars->full_v[sv], C::kTile);
+        load_tile<D>(sV + sv * C::kTile, &tmV, &bars->full_v[sv], 128 * s, bkv);
       }
       if (!ok) bwd_record(p.status);
-      for (int s = max(0, nsteps - kStages); s < nsteps; ++s)
-        (void)mbar_wait(&bars->full[s % kStages], (s / kStages) & 1);
+      for (int s = max(0, nsteps - kKStages); s < nsteps; ++s)
+        (void)mbar_wait(&bars->full[s % kKStages], (s / kKStages) & 1);
+      for (int s = max(0, nsteps - kVStages); s < nsteps; ++s)
+        (void)mbar_wait(&bars->full_v[s % kVStages], (s / kVStages) & 1);
       (void)mbar_wait(&bars->fixed_full, 0);
     }
   } else if (warp == kBwdMmaWarp) {
     if (lane == 0 && nsteps > 0) {
       ok = bwd_wait(&bars->fixed_full, 0, bars);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+      auto issue_s = [&](int s) -> bool {  // S = Q K^T
+        const int sk = s % kKStages;
+        if (!bwd_wait(&bars->full[sk], (s / kKStages) & 1, bars)) return false;
+        mma_ss_tile<D>(tmem, C::kColS, q_addr, k_base + sk * C::kTile);
+        tc_commit(&bars->s_full);
+        return true;
+      };
+      auto issue_dp = [&](int s) -> bool {  // dP = dO V^T; V(s) is free afterwards
+        const int sv = s % kVStages;
+        if (!bwd_wait(&bars->full_v[sv], (s / kVStages) & 1, bars)) return false;
+        mma_ss_tile<D>(tmem, C::kColDP, do_addr, v_base + sv * C::kTile);
+        tc_commit(&bars->dp_full);
+        tc_commit(&bars->empty_v[sv]);
+        return true;
+      };
+      if (ok) ok = issue_s(0) && issue_dp(0);
       for (int s = 0; s < nsteps && ok; ++s) {
-        const int st = s % kStages;
-        if (!(ok = bwd_wait(&bars->full[st], (s / kStages) & 1, bars))) break;
-        const uint32_t k_addr = smem_u32(sRing + st * 2 * C::kTile);
-        const uint32_t v_addr = k_addr + C::kTile;
-        // S = Q K^T and dP = dO V^T
-        mma_two_ss<D>(tmem, q_addr, k_addr, do_addr, v_addr);
-        tc_commit(&bars->sd_full);
-        if (!(ok = bwd_wait(&bars->p_full, s & 1, bars))) break;
+        // S(s+1) as soon as the gradient warps have read S(s) ...
+        if (s + 1 < nsteps) {
+          if (!(ok = bwd_wait(&bars->p_ready, s & 1, bars))) break;
+          tc_fence_after();
+          if (!(ok = issue_s(s + 1))) break;
+        }
+        // ... dQ += dS K once dS(s) is in TMEM (K MN-major: its rows are the K dim) ...
+        if (!(ok = bwd_wait(&bars->ds_full, s & 1, bars))) break;
         tc_fence_after();
-        // dQ += dS K (K MN-major: its rows are the K dim)
-        mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, k_addr, s == 0);
-        tc_commit(&bars->empty[st]);
+        mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, k_base + (s % kKStages) * C::kTile, s == 0);
+        tc_commit(&bars->empty[s % kKStages]);
+        // ... then dP(s+1), which overwrites dS(s) after dQ has read it.
+        if (s + 1 < nsteps && !(ok = issue_dp(s + 1))) break;
       }
       if (ok) tc_commit(&bars->acc_full);
       if (!ok) bwd_record(p.status);
@@ -510,35 +621,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float lse2 = row_valid ? __ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e
                                  : 0.f;
     const float dlt = row_valid ? __ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
+    const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t nl2 = f2_pack(-lse2, -lse2);
+    const uint64_t ndl = f2_pack(-dlt, -dlt);
     const int key_hi = p.causal ? min(p.Sk - 1, row + p.Sk - p.Sq) : p.Sk - 1;
     for (int s = 0; s < nsteps && ok; ++s) {
-      ok = __all_sync(0xffffffffu, bwd_wait(&bars->sd_full, s & 1, bars));
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->s_full, s & 1, bars));
       if (!ok) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_addr + C::kColS + 32 * c, sr);
-        tmem_ld32(tmem + lane_addr + C::kColDP + 32 * c, dr);
+      uint32_t sr[64];
+      tmem_ld32(tmem + lane_addr + C::kColS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld32(tmem + lane_addr + C::kColS + 64 * half + 32,
+                *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      // S(s) is in registers: its columns may be overwritten by S(s+1).
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // Keys 128s + 64*half + e are visible for e < n_vis (causal limit, Sk).
+      const int n_vis = row_valid ? min(max(key_hi - (128 * s + 64 * half) + 1, 0), 64) : 0;
+      const bool need_mask = __any_sync(0xffffffffu, n_vis < 64);
+      float pv[64];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2, nl2),
+                  x0, x1);
+        float p0 = ex2(x0), p1 = ex2(x1);
+        if (need_mask) {
+          p0 = e < n_vis ? p0 : 0.f;
+          p1 = e + 1 < n_vis ? p1 : 0.f;
+        }
+        pv[e] = p0;
+        pv[e + 1] = p1;
+      }
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->dp_full, s & 1, bars));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t dr[32];
+        tmem_ld32(tmem + lane_addr + C::kColDP + 64 * half + 32 * cc, dr);
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int key = 128 * s + 32 * c + e + u;
-            const bool vis = row_valid && key <= key_hi;
-            const float x = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -lse2);
-            const float pv = vis ? ex2(x) : 0.f;
-            dv[u] = pv * (__uint_as_float(dr[e + u]) - dlt);
-          }
-          dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(pv[32 * cc + e], pv[32 * cc + e + 1]),
+                           f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                  ndl)),
+                    d0, d1);
+          dk[e >> 1] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(tmem + lane_addr + C::kColDP + 64 * half + 16 * (c - 2 * half), dk);
+        tmem_st16(tmem + lane_addr + C::kColDP + 64 * half + 16 * cc, dk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->ds_full);
     }
     if (ok) {
       float* dq_row = p.out0 + (static_cast<size_t>(bh) * p.Sq + row) * D;
@@ -588,7 +724,7 @@ cudaError_t launch_bwd_impl(const void* q, const void* k, const void* v, const f
                             static_cast<int>(C::kSmem))) != cudaSuccess)
     return e;
   if ((e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dq_kernel<D>),
-                            static_cast<int>(C::kSmem))) != cudaSuccess)
+                            static_cast<int>(C::kSmemDq))) != cudaSuccess)
     return e;
   BwdParams p;
   p.lse = lse;
@@ -610,7 +746,7 @@ cudaError_t launch_bwd_impl(const void* q, const void* k, const void* v, const f
   p.out0 = dq;
   p.out1 = nullptr;
   const int q_ctas = B * Hq * ((Sq + 127) / 128);
-  bwd_dq_kernel<D><<<q_ctas, kBwdThreads, C::kSmem, stream>>>(tmQ, tmK, tmV, tmDO, p);
+  bwd_dq_kernel<D><<<q_ctas, kBwdThreads, C::kSmemDq, stream>>>(tmQ, tmK, tmV, tmDO, p);
   return cudaGetLastError();
 }
 
