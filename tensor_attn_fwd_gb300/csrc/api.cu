@@ -30,7 +30,8 @@ struct AttrEntry {
   int bytes;
   uint64_t device_mask;
 };
-AttrEntry g_attr[16];
+constexpr int kAttrSlots = 32;  // one per kernel instantiation that sets its shared memory size
+AttrEntry g_attr[kAttrSlots];
 int g_attr_n = 0;
 
 int current_device() {
@@ -84,7 +85,7 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err != cudaSuccess) return err;
   if (e == nullptr) {
-    if (g_attr_n >= 16) return cudaSuccess;  // table full: set again next time
+    if (g_attr_n >= kAttrSlots) return cudaSuccess;  // table full: set again next time
     e = &g_attr[g_attr_n++];
     e->kernel = kernel;
     e->bytes = bytes;
