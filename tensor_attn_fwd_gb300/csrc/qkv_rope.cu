@@ -11,11 +11,21 @@
 //   (a, b) -> (a cos - b sin, a sin + b cos)
 // on dims (2i, 2i+1) (style 0) or (i, i + D/2) (style 1), for Q and K heads.
 //
-// GEMM  Y[T, N] = X[T, hidden] W[N, hidden]^T,  N = (Hq + 2 Hkv) D, on tcgen05:
-//   tile 128 tokens x 256 features, K in steps of 64 (one 128B-swizzled box),
-//   4-stage TMA ring (A 16 KB + B 32 KB per stage), fp32 accumulator in TMEM,
-//   two accumulator buffers (2 x 256 columns) so that the epilogue of one tile
-//   overlaps the MMAs of the next.  Persistent grid, one CTA per SM.
+// GEMM  Y[T, N] = X[T, hidden] W[N, hidden]^T,  N = (Hq + 2 Hkv) D, on tcgen05,
+// K in steps of 64 (one 128B-swizzled box), fp32 accumulator in TMEM, two
+// accumulator buffers (2 x 256 columns) so that the epilogue of one tile
+// overlaps the MMAs of the next.  Persistent grid, one CTA per SM.  Two forms:
+//   single  tile 128 tokens x 256 features per CTA; 4-stage ring of
+//           A 16 KB + B 32 KB.
+//   pair    a cluster of two CTAs on neighbouring SMs computes 256 tokens x
+//           256 features with tcgen05.mma.cta_group::2 (M = 256) issued by the
+//           even CTA: each CTA stages its own 128 token rows of X and half of
+//           the 256 weight rows (N is split across the pair), so a stage is
+//           A 16 KB + B 16 KB per SM (6 stages) for the same work per SM --
+//           a third less shared-memory fill per FLOP.  Full barriers live in
+//           the even CTA and count both CTAs' copies; MMA completions are
+//           multicast to both CTAs; both CTAs' epilogue threads release an
+//           accumulator buffer on the even CTA's barrier.
 // Roles (192 threads): warp 0 TMA (one thread), warp 1 MMA (one thread),
 // warps 2-5 epilogue (thread = token row = TMEM lane): tcgen05.ld of the
 // accumulator, rotation with a (cos, sin) table, bf16 rounding, store into
@@ -36,18 +46,24 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kGStages = 4;
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // rows per CTA, features per tile, K step
 constexpr int kGThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr size_t kGSmem = 1024 + size_t(kGStages) * kStageBytes + 256;
-static_assert(kGSmem <= 232448, "shared memory per CTA");
-constexpr uint32_t kIdescG = idesc_bf16_f32(kBM, kBN, false, false);
+
+template <bool kPair>
+struct GCfg {
+  static constexpr uint32_t kBRows = kPair ? kBN / 2 : kBN;  // weight rows staged per CTA
+  static constexpr uint32_t kBBytes = kBRows * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + 256;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kPair ? 2 * kBM : kBM, kBN, false, false);
+};
+constexpr int kGMaxStages = 6;
 
 struct GBars {
-  uint64_t full[kGStages], empty[kGStages];
+  uint64_t full[kGMaxStages], empty[kGMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -70,14 +86,18 @@ __device__ __forceinline__ void gnote(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Bounded wait; in the pair form barriers are also signalled from the peer
+// CTA, so the wait acquires at cluster scope.
+template <bool kPair>
 __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, GBars* bars) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto probe = [&] { return kPair ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(a, parity)) return true;
+      if (probe()) return true;
     if (*reinterpret_cast<volatile int*>(&bars->abort)) return false;
     if (globaltimer() - t0 > ATTN_WAIT_NS) {
       *reinterpret_cast<volatile int*>(&bars->abort) = 1;
@@ -86,65 +106,109 @@ __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, GBars* bar
   }
 }
 
+// Work slots: one per CTA (single) or one per CTA pair.
+template <bool kPair>
+__device__ __forceinline__ int g_slot() {
+  return kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+}
+template <bool kPair>
+__device__ __forceinline__ int g_slots() {
+  return kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+}
+
+template <bool kPair>
 __device__ void g_load(const CUtensorMap* tmX, const CUtensorMap* tmW, const QkvParams& p,
                        uint8_t* ring, GBars* bars) {
+  using C = GCfg<kPair>;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   uint32_t ctr = 0;
   bool ok = true;
   const int total = p.mt * p.nt;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-    const int m0 = (t / p.nt) * kBM, n0 = (t % p.nt) * kBN;
+  for (int t = g_slot<kPair>(); t < total && ok; t += g_slots<kPair>()) {
+    const int m0 = (t / p.nt) * (kPair ? 2 * kBM : kBM) + int(rank) * kBM;
+    const int n0 = (t % p.nt) * kBN + int(rank) * int(C::kBRows);
     for (int kb = 0; kb < p.kb; ++kb) {
-      const uint32_t st = ctr % kGStages;
-      if (ctr >= uint32_t(kGStages) &&
-          !(ok = gwait(&bars->empty[st], ((ctr / kGStages) - 1) & 1, bars)))
+      const uint32_t st = ctr % C::kStages;
+      if (ctr >= uint32_t(C::kStages) &&
+          !(ok = gwait<kPair>(&bars->empty[st], ((ctr / C::kStages) - 1) & 1, bars)))
         break;
-      uint8_t* sA = ring + st * kStageBytes;
-      mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
-      tma_load_3d(sA, tmX, &bars->full[st], kb * kBK, m0, 0);
-      tma_load_3d(sA + kABytes, tmW, &bars->full[st], kb * kBK, n0, 0);
+      uint8_t* sA = ring + st * C::kStageBytes;
+      if constexpr (kPair) {
+        // The even CTA's barrier counts both CTAs' bytes.
+        if (rank == 0) mbar_arrive_expect_tx(&bars->full[st], 2 * C::kStageBytes);
+        const uint32_t fb = mapa_shared(smem_u32(&bars->full[st]), 0);
+        tma_load_3d_pair(sA, tmX, fb, kb * kBK, m0, 0);
+        tma_load_3d_pair(sA + kABytes, tmW, fb, kb * kBK, n0, 0);
+      } else {
+        mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
+        tma_load_3d(sA, tmX, &bars->full[st], kb * kBK, m0, 0);
+        tma_load_3d(sA + kABytes, tmW, &bars->full[st], kb * kBK, n0, 0);
+      }
       ++ctr;
     }
   }
   if (!ok) gnote(p.status, ATTN_ERR_TIMEOUT);
-  for (uint32_t c = (ctr > uint32_t(kGStages) ? ctr - kGStages : 0); c < ctr; ++c)
-    (void)mbar_wait(&bars->full[c % kGStages], (c / kGStages) & 1);
+  // Let every copy issued land before the CTA can exit (in the pair form the
+  // even CTA's barriers count both CTAs' copies, and the closing cluster
+  // barrier keeps the odd CTA alive until then).
+  if (rank == 0)
+    for (uint32_t c = (ctr > uint32_t(C::kStages) ? ctr - C::kStages : 0); c < ctr; ++c)
+      (void)mbar_wait(&bars->full[c % C::kStages], (c / C::kStages) & 1);
 }
 
+template <bool kPair>
 __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t tmem) {
+  using C = GCfg<kPair>;
   constexpr uint64_t kDesc = sdesc_sw128(0, 16, 1024);  // K-major, 128B swizzle
   constexpr uint32_t kHi = static_cast<uint32_t>(kDesc >> 32);
   const uint32_t lo0 = static_cast<uint32_t>(kDesc) + (smem_u32(ring) >> 4);
+  auto commit = [&](uint64_t* bar) {  // completion to both CTAs of a pair
+    if constexpr (kPair)
+      tc_commit_pair_mc(smem_u32(bar), 0x3);
+    else
+      tc_commit(bar);
+  };
   uint32_t ctr = 0, i = 0;
   bool ok = true;
   const int total = p.mt * p.nt;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+  for (int t = g_slot<kPair>(); t < total && ok; t += g_slots<kPair>(), ++i) {
     const uint32_t a = i & 1;
-    if (i >= 2 && !(ok = gwait(&bars->acc_empty[a], ((i >> 1) - 1) & 1, bars))) break;
+    if (i >= 2 && !(ok = gwait<kPair>(&bars->acc_empty[a], ((i >> 1) - 1) & 1, bars))) break;
     tc_fence_after();
     const uint32_t d = tmem + a * kBN;
     for (int kb = 0; kb < p.kb; ++kb) {
-      const uint32_t st = ctr % kGStages;
-      if (!(ok = gwait(&bars->full[st], (ctr / kGStages) & 1, bars))) break;
+      const uint32_t st = ctr % C::kStages;
+      if (!(ok = gwait<kPair>(&bars->full[st], (ctr / C::kStages) & 1, bars))) break;
       tc_fence_after();
-      const uint32_t sa = lo0 + ((st * kStageBytes) >> 4);
+      const uint32_t sa = lo0 + ((st * C::kStageBytes) >> 4);
       const uint32_t sb = sa + (kABytes >> 4);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         const uint64_t ad = desc_from_words(sa + ((kk * 32) >> 4), kHi);
         const uint64_t bd = desc_from_words(sb + ((kk * 32) >> 4), kHi);
-        if (kb == 0 && kk == 0)
-          mma_ss_c<0>(d, ad, bd, kIdescG);
-        else
-          mma_ss_c<1>(d, ad, bd, kIdescG);
+        if constexpr (kPair) {
+          if (kb == 0 && kk == 0)
+            mma_ss_pair<0>(d, ad, bd, C::kIdesc);
+          else
+            mma_ss_pair<1>(d, ad, bd, C::kIdesc);
+        } else {
+          if (kb == 0 && kk == 0)
+            mma_ss_c<0>(d, ad, bd, C::kIdesc);
+          else
+            mma_ss_c<1>(d, ad, bd, C::kIdesc);
+        }
       }
-      tc_commit(&bars->empty[st]);
+      commit(&bars->empty[st]);
       ++ctr;
     }
     if (!ok) break;
-    tc_commit(&bars->acc_full[a]);
+    commit(&bars->acc_full[a]);
   }
   if (!ok) gnote(p.status, ATTN_ERR_TIMEOUT);
-  tc_commit(&bars->mma_done);
+  if constexpr (kPair)
+    tc_commit_pair_mc(smem_u32(&bars->mma_done), 0x1);
+  else
+    tc_commit(&bars->mma_done);
   (void)mbar_wait(&bars->mma_done, 0);
 }
 
@@ -161,19 +225,22 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* x)
   }
 }
 
+template <bool kPair>
 __device__ void g_epilogue(const QkvParams& p, GBars* bars, uint32_t tmem, int warp, int lane) {
   const int quarter = warp & 3;  // TMEM lanes this warp may access
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
   const int half = p.D / 2;
   uint32_t i = 0;
   bool ok = true;
   const int total = p.mt * p.nt;
-  for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+  for (int t = g_slot<kPair>(); t < total && ok; t += g_slots<kPair>(), ++i) {
     const uint32_t a = i & 1;
-    ok = __all_sync(0xffffffffu, gwait(&bars->acc_full[a], (i >> 1) & 1, bars));
+    ok = __all_sync(0xffffffffu, gwait<kPair>(&bars->acc_full[a], (i >> 1) & 1, bars));
     if (!ok) break;
     tc_fence_after();
-    const int m0 = (t / p.nt) * kBM, n0 = (t % p.nt) * kBN;
+    const int m0 = (t / p.nt) * (kPair ? 2 * kBM : kBM) + int(rank) * kBM;
+    const int n0 = (t % p.nt) * kBN;
     const int row = m0 + quarter * 32 + lane;
     const bool valid = row < p.T;
     int b = 0, s = 0, pos = 0;
@@ -252,60 +319,80 @@ __device__ void g_epilogue(const QkvParams& p, GBars* bars, uint32_t tmem, int w
       }
     }
     // Every tcgen05.ld of this buffer has completed (each waits); the MMA
-    // warp may reuse it.
+    // warp may reuse it (in the pair form: the even CTA's barrier).
     tc_fence_before();
-    mbar_arrive(&bars->acc_empty[a]);
+    if constexpr (kPair)
+      mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[a]), 0));
+    else
+      mbar_arrive(&bars->acc_empty[a]);
   }
   if (!ok) gnote(p.status, ATTN_ERR_TIMEOUT);
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kGThreads, 1)
     qkv_rope_kernel(const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmW, const QkvParams p) {
+  using C = GCfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  GBars* bars = reinterpret_cast<GBars*>(ring + kGStages * kStageBytes);
+  GBars* bars = reinterpret_cast<GBars*>(ring + C::kStages * C::kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const bool mma_cta = !kPair || cluster_ctarank() == 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bars->acc_full[a], 1);
-      mbar_init(&bars->acc_empty[a], 128);
+      mbar_init(&bars->acc_empty[a], kPair ? 256 : 128);  // every epilogue thread (of the pair)
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(&bars->tmem_base, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_base, 512);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();  // both CTAs' barriers are initialised before any remote use
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (warp == 0) {
-    if (lane == 0) g_load(&tmX, &tmW, p, ring, bars);
+    if (lane == 0) g_load<kPair>(&tmX, &tmW, p, ring, bars);
   } else if (warp == 1) {
-    if (lane == 0) g_mma(p, ring, bars, tmem);
+    if (lane == 0 && mma_cta) g_mma<kPair>(p, ring, bars, tmem);
   } else {
-    g_epilogue(p, bars, tmem, warp, lane);
+    g_epilogue<kPair>(p, bars, tmem, warp, lane);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  else
+    __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
 }
 
@@ -353,19 +440,54 @@ cudaError_t launch_qkv_rope(const void* x, const void* w, const float* rope, con
   p.N = (Hq + 2 * Hkv) * D;
   p.max_pos = max_pos;
   p.style = style;
-  p.mt = (p.T + kBM - 1) / kBM;
   p.nt = (p.N + kBN - 1) / kBN;
   p.kb = (hidden + kBK - 1) / kBK;
+  // CTA pairs once there are at least 512 tokens (two 256-row tiles).
+  const bool pair = p.T >= 4 * kBM;
   CUtensorMap tmX, tmW;
   if (!encode_bf16_map(&tmX, x, hidden, p.T, 1, kBM) ||
-      !encode_bf16_map(&tmW, w, hidden, p.N, 1, kBN))
+      !encode_bf16_map(&tmW, w, hidden, p.N, 1, pair ? kBN / 2 : kBN))
     return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(qkv_rope_kernel),
-                                   static_cast<int>(kGSmem));
+  if (!pair) {
+    p.mt = (p.T + kBM - 1) / kBM;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(qkv_rope_kernel<false>),
+                                     static_cast<int>(GCfg<false>::kSmem));
+    if (e != cudaSuccess) return e;
+    const int total = p.mt * p.nt;
+    const int grid = total < sm_count() ? total : sm_count();
+    qkv_rope_kernel<false><<<grid, kGThreads, GCfg<false>::kSmem, stream>>>(tmX, tmW, p);
+    return cudaGetLastError();
+  }
+  p.mt = (p.T + 2 * kBM - 1) / (2 * kBM);
+  const void* kernel = reinterpret_cast<const void*>(qkv_rope_kernel<true>);
+  cudaError_t e = ensure_smem_attr(kernel, static_cast<int>(GCfg<true>::kSmem));
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kGThreads, 1, 1);
+  cfg.dynamicSmemBytes = GCfg<true>::kSmem;
+  cfg.stream = stream;
+  static int max_clusters[64] = {0};  // clusters of two resident at once, per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    cfg.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0)
+      n = sm_count() / 2;
+    max_clusters[dev] = n;
+  }
   const int total = p.mt * p.nt;
-  const int grid = total < sm_count() ? total : sm_count();
-  qkv_rope_kernel<<<grid, kGThreads, kGSmem, stream>>>(tmX, tmW, p);
+  const int clusters = total < max_clusters[dev] ? total : max_clusters[dev];
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, qkv_rope_kernel<true>, tmX, tmW, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

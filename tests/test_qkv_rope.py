@@ -66,6 +66,8 @@ def test_qkv_rope_ragged_sizes():
     # N = (3 + 2) * 64 = 320 (not a multiple of 256).
     run_case(3, 77, 200, 3, 1, 64, 0, seed=11)
     run_case(1, 1, 8, 1, 1, 128, 1, seed=12)
+    # CTA-pair form (T >= 512): T = 700 (2 x 256 + 188), hidden 200, N = 320.
+    run_case(1, 700, 200, 3, 1, 64, 1, seed=13)
 
 
 def test_qkv_rope_positions_and_gqa():
