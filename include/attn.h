@@ -194,6 +194,20 @@ ATTN_API int attn_qkv_rope(const void *x, const void *w, const float *rope_table
                            void *stream);
 
 /*
+ * A split count for attn_decode_splitkv (and its varlen / paged forms) on the
+ * current device.  The pages leave the split count to the caller; this is a
+ * measured rule for this library's decode kernel, not part of the method.
+ * With B * Hkv * ceil((Hq/Hkv) / 16) CTAs per split already filling at least
+ * 80 % of the SMs, one split streams K/V fastest; otherwise about one CTA per
+ * SM, with at least 1024 keys per split.  Host-only: launches nothing.
+ *
+ *   *num_splits receives the count (>= 1, <= max(1, Sk / 1024)).
+ *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0,
+ *   ATTN_ERR_CUDA if the device cannot be queried.
+ */
+ATTN_API int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int *num_splits);
+
+/*
  * Split-KV decode, second stage: log-sum-exp combine of the partials.
  * Source: same page (FlashDecoding's reduction across key splits).
  *   lse = ln sum_s exp(lse_s);  o = sum_s exp(lse_s - lse) * o_s

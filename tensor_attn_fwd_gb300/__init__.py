@@ -32,7 +32,7 @@ import torch
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
            "attn_decode_splitkv_paged", "attn_combine", "decode", "decode_paged", "attn_bwd",
-           "attn_rope_table", "attn_qkv_rope",
+           "attn_rope_table", "attn_qkv_rope", "attn_decode_num_splits",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
            "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
@@ -66,6 +66,7 @@ _SIGNATURES = {
     "attn_decode_splitkv_paged": ([_vp] * 7 + [_int] * 8 + [_flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
     "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
+    "attn_decode_num_splits": ([_int, _int, _int, _int, ctypes.POINTER(_int)], _int),
     "attn_qkv_rope": ([_vp] * 7 + [_int] * 8 + [_vp], _int),
     "attn_bwd": ([_vp] * 10 + [_int] * 7 + [_flt, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
@@ -401,13 +402,27 @@ def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor |
     return o, lse
 
 
-def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
+def attn_decode_num_splits(B: int, Hq: int, Hkv: int, Sk: int, device=None) -> int:
+    """Split count for the decode kernels on ``device`` (measured rule, host only)."""
+    lib = load_library()
+    n = _int(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = lib.attn_decode_num_splits(int(B), int(Hq), int(Hkv), int(Sk), ctypes.byref(n))
+    _raise_if(st, "attn_decode_num_splits")
+    return int(n.value)
+
+
+def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int | None = None,
            scale: float | None = None, workspace=None, o=None, lse=None, stream=None,
            seqlens: torch.Tensor | None = None):
     """Split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq]).
 
     With ``seqlens`` (int32 CUDA [B]) sequence b attends to its first seqlens[b] keys.
+    ``num_splits=None`` picks attn_decode_num_splits for the shape.
     """
+    if num_splits is None:
+        num_splits = attn_decode_num_splits(q.shape[0], q.shape[1], k.shape[1], k.shape[2],
+                                            q.device)
     o_part, lse_part = (None, None) if workspace is None else workspace
     if seqlens is None:
         o_part, lse_part = attn_decode_splitkv(q, k, v, num_splits, scale, o_part, lse_part,

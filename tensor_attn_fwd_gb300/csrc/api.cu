@@ -328,6 +328,25 @@ int attn_qkv_rope(const void* x, const void* w, const float* rope_table, const i
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int* num_splits) {
+  if (num_splits == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return ATTN_ERR_CUDA;
+  // CTAs without splitting: (batch, KV head, 16-head slice of the group).
+  const long long base = static_cast<long long>(B) * Hkv * ((Hq / Hkv + 15) / 16);
+  long long ns = 1;
+  if (base * 5 < static_cast<long long>(n_sm) * 4) {
+    // Too few to stream at full bandwidth: about one CTA per SM, each split
+    // keeping at least 1024 keys.
+    ns = (n_sm + base - 1) / base;
+    const long long cap = Sk / 1024 > 1 ? Sk / 1024 : 1;
+    if (ns > cap) ns = cap;
+  }
+  *num_splits = static_cast<int>(ns);
+  return ATTN_OK;
+}
+
 int attn_combine(const float* o_part, const float* lse_part, float* o, float* lse, int B, int Hq,
                  int D, int num_splits, void* stream) {
   if (!o_part || !lse_part || !o || !lse) return ATTN_ERR_INVALID_ARG;

@@ -204,3 +204,10 @@ def test_qkv_rope_rejects(lib, kw, code):
 ])
 def test_rope_table_rejects(lib, args, code):
     assert lib.attn_rope_table(*args, None) == code
+
+
+def test_decode_num_splits_rejects(lib):
+    n = ctypes.c_int(0)
+    assert lib.attn_decode_num_splits(1, 4, 1, 64, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_num_splits(0, 4, 1, 64, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_num_splits(1, 6, 4, 64, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG

@@ -265,3 +265,24 @@ def test_bf16_output(B, Hq, Hkv, Sq, Sk, D, causal):
     # exactly the fp32 result rounded to nearest even
     assert torch.equal(o16, o32.to(torch.bfloat16))
     assert torch.equal(lse, lse32)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sk,want", [
+    (64, 32, 8, 4096, 1),      # 512 CTAs already fill the SMs
+    (4, 32, 8, 8192, None),    # 32 CTAs: several splits
+    (1, 32, 8, 2048, 2),       # capped at Sk / 1024
+    (1, 4, 1, 500, 1),         # too short to split
+])
+def test_decode_num_splits_rule(B, Hq, Hkv, Sk, want):
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = attn.attn_decode_num_splits(B, Hq, Hkv, Sk)
+    base = B * Hkv * (((Hq // Hkv) + 15) // 16)
+    expect = want if want is not None else min((n_sm + base - 1) // base, max(1, Sk // 1024))
+    assert ns == expect
+    # and the default decode path uses it and matches the oracle
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, 128, seed=B + Sk)
+    o, lse = attn.decode(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(128))
+    assert_close(o.cpu().numpy(), lse.cpu().numpy(), o_ref[:, :, 0], lse_ref[:, :, 0], "auto splits")
