@@ -485,7 +485,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
 
 
 def profile_arm(args):
-    """A short run of one path for ncu: `--profile prefill|decode|backward|qkv`, no
+    """A short run of one path for ncu: `--profile prefill|decode|backward|qkv|d256`, no
     flush, no e2e, no CPU baseline; `--batch` shrinks the workload's batch.
     `backward` runs one forward, then the Delta, dK/dV and dQ kernels per step."""
     import dataclasses
@@ -496,7 +496,8 @@ def profile_arm(args):
     w = DECODE if args.profile == "decode" else PREFILL
     if args.batch:
         w = dataclasses.replace(w, B=args.batch)
-    q, k, v = (t.to(device) for t in workload_inputs(w))
+    if args.profile != "d256":
+        q, k, v = (t.to(device) for t in workload_inputs(w))
     if args.profile == "prefill":
         def fn():
             attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
@@ -511,6 +512,16 @@ def profile_arm(args):
 
         def fn():
             attn.attn_qkv_rope(xq, wq, table, w.Hq, w.Hkv)
+    elif args.profile == "d256":
+        # head dimension 256: causal GQA Hq16 Hkv4 S8192 (batch from --batch, default 2)
+        from attn_inputs import make_qkv
+        bsz = args.batch or 2
+        q, k, v = (t.to(device) for t in make_qkv(bsz, 16, 4, 8192, 8192, 256, seed=2561))
+        w = dataclasses.replace(w, name="gqa_hq16_hkv4_s8192_d256_causal", B=bsz, Hq=16, Hkv=4,
+                                D=256)
+
+        def fn():
+            attn.attn_fwd(q, k, v, causal=True, scale=1.0 / 16.0)
     elif args.profile == "backward":
         o, lse = attn.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
         g = torch.Generator().manual_seed(w.seed + 7)
@@ -541,7 +552,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-qkv-rope", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["prefill", "decode", "backward", "qkv"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward", "qkv", "d256"], default=None,
                     help="run a few launches of one kernel (for ncu) and exit")
     ap.add_argument("--batch", type=int, default=0, help="override B in --profile mode")
     args = ap.parse_args()
