@@ -16,13 +16,14 @@
 // accumulator buffers (2 x 256 columns) so that the epilogue of one tile
 // overlaps the MMAs of the next.  Persistent grid, one CTA per SM.  Two forms:
 //   single  tile 128 tokens x 256 features per CTA; 4-stage ring of
-//           A 16 KB + B 32 KB.
+//           A 16 KB + B 32 KB (K = 64 per stage).
 //   pair    a cluster of two CTAs on neighbouring SMs computes 256 tokens x
 //           256 features with tcgen05.mma.cta_group::2 (M = 256) issued by the
 //           even CTA: each CTA stages its own 128 token rows of X and half of
-//           the 256 weight rows (N is split across the pair), so a stage is
-//           A 16 KB + B 16 KB per SM (6 stages) for the same work per SM --
-//           a third less shared-memory fill per FLOP.  Full barriers live in
+//           the 256 weight rows (N is split across the pair), so K = 64 costs
+//           A 16 KB + B 16 KB per SM for the same work per SM -- a third less
+//           shared-memory fill per FLOP.  A stage holds K = 128 (3 stages of
+//           64 KB), i.e. 8 MMAs per barrier wait and commit.  Full barriers live in
 //           the even CTA and count both CTAs' copies; MMA completions are
 //           multicast to both CTAs; both CTAs' epilogue threads release an
 //           accumulator buffer on the even CTA's barrier.
@@ -46,16 +47,22 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;  // rows per CTA, features per tile, K step
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // rows per CTA, features per tile, TMA box K
 constexpr int kGThreads = 192;
-constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kASub = kBM * kBK * 2;  // one [128 rows x 64] A box: 16 KB
 
 template <bool kPair>
 struct GCfg {
   static constexpr uint32_t kBRows = kPair ? kBN / 2 : kBN;  // weight rows staged per CTA
-  static constexpr uint32_t kBBytes = kBRows * kBK * 2;
+  // K per stage: two 64-wide boxes per operand in the pair form (8 MMAs per
+  // barrier wait and commit), one in the single form.
+  static constexpr int kSubK = kPair ? 2 : 1;
+  static constexpr int kStageK = kSubK * kBK;
+  static constexpr uint32_t kBSub = kBRows * kBK * 2;
+  static constexpr uint32_t kABytes = kSubK * kASub;
+  static constexpr uint32_t kBBytes = kSubK * kBSub;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kStages = kPair ? 3 : 4;
   static constexpr size_t kSmem = 1024 + size_t(kStages) * kStageBytes + 256;
   static_assert(kSmem <= 232448, "shared memory per CTA");
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kPair ? 2 * kBM : kBM, kBN, false, false);
@@ -133,16 +140,25 @@ __device__ void g_load(const CUtensorMap* tmX, const CUtensorMap* tmW, const Qkv
           !(ok = gwait<kPair>(&bars->empty[st], ((ctr / C::kStages) - 1) & 1, bars)))
         break;
       uint8_t* sA = ring + st * C::kStageBytes;
+      // Boxes past `hidden` are zero-filled by TMA and still deliver their bytes.
       if constexpr (kPair) {
         // The even CTA's barrier counts both CTAs' bytes.
         if (rank == 0) mbar_arrive_expect_tx(&bars->full[st], 2 * C::kStageBytes);
         const uint32_t fb = mapa_shared(smem_u32(&bars->full[st]), 0);
-        tma_load_3d_pair(sA, tmX, fb, kb * kBK, m0, 0);
-        tma_load_3d_pair(sA + kABytes, tmW, fb, kb * kBK, n0, 0);
+#pragma unroll
+        for (int sub = 0; sub < C::kSubK; ++sub) {
+          const int x = kb * C::kStageK + sub * kBK;
+          tma_load_3d_pair(sA + sub * kASub, tmX, fb, x, m0, 0);
+          tma_load_3d_pair(sA + C::kABytes + sub * C::kBSub, tmW, fb, x, n0, 0);
+        }
       } else {
         mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
-        tma_load_3d(sA, tmX, &bars->full[st], kb * kBK, m0, 0);
-        tma_load_3d(sA + kABytes, tmW, &bars->full[st], kb * kBK, n0, 0);
+#pragma unroll
+        for (int sub = 0; sub < C::kSubK; ++sub) {
+          const int x = kb * C::kStageK + sub * kBK;
+          tma_load_3d(sA + sub * kASub, tmX, &bars->full[st], x, m0, 0);
+          tma_load_3d(sA + C::kABytes + sub * C::kBSub, tmW, &bars->full[st], x, n0, 0);
+        }
       }
       ++ctr;
     }
@@ -181,11 +197,12 @@ __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t t
       if (!(ok = gwait<kPair>(&bars->full[st], (ctr / C::kStages) & 1, bars))) break;
       tc_fence_after();
       const uint32_t sa = lo0 + ((st * C::kStageBytes) >> 4);
-      const uint32_t sb = sa + (kABytes >> 4);
+      const uint32_t sb = sa + (C::kABytes >> 4);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t ad = desc_from_words(sa + ((kk * 32) >> 4), kHi);
-        const uint64_t bd = desc_from_words(sb + ((kk * 32) >> 4), kHi);
+      for (int kk = 0; kk < C::kStageK / 16; ++kk) {
+        const int sub = kk >> 2;
+        const uint64_t ad = desc_from_words(sa + ((sub * kASub + (kk & 3) * 32) >> 4), kHi);
+        const uint64_t bd = desc_from_words(sb + ((sub * C::kBSub + (kk & 3) * 32) >> 4), kHi);
         if constexpr (kPair) {
           if (kb == 0 && kk == 0)
             mma_ss_pair<0>(d, ad, bd, C::kIdesc);
@@ -441,9 +458,10 @@ cudaError_t launch_qkv_rope(const void* x, const void* w, const float* rope, con
   p.max_pos = max_pos;
   p.style = style;
   p.nt = (p.N + kBN - 1) / kBN;
-  p.kb = (hidden + kBK - 1) / kBK;
   // CTA pairs once there are at least 512 tokens (two 256-row tiles).
   const bool pair = p.T >= 4 * kBM;
+  const int stage_k = pair ? GCfg<true>::kStageK : GCfg<false>::kStageK;
+  p.kb = (hidden + stage_k - 1) / stage_k;
   CUtensorMap tmX, tmW;
   if (!encode_bf16_map(&tmX, x, hidden, p.T, 1, kBM) ||
       !encode_bf16_map(&tmW, w, hidden, p.N, 1, pair ? kBN / 2 : kBN))

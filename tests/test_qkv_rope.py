@@ -68,6 +68,9 @@ def test_qkv_rope_ragged_sizes():
     run_case(1, 1, 8, 1, 1, 128, 1, seed=12)
     # CTA-pair form (T >= 512): T = 700 (2 x 256 + 188), hidden 200, N = 320.
     run_case(1, 700, 200, 3, 1, 64, 1, seed=13)
+    # hidden 64: the second 64-wide box of every K = 128 stage lies wholly past
+    # hidden and must arrive as zeros.
+    run_case(2, 300, 64, 2, 1, 128, 0, seed=14)
 
 
 def test_qkv_rope_positions_and_gqa():
