@@ -202,6 +202,8 @@ int decode_common(const void* q, const void* k, const void* v, const int* seqlen
   if (paged == nullptr && static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
     return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
+  // Output rows (and tensor-map planes) are indexed with int.
+  if (static_cast<long long>(B) * Hq > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
   const int head_slices = (Hq / Hkv + 15) / 16;  // query heads per decode CTA: 16
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535)
     return ATTN_ERR_UNSUPPORTED;
@@ -276,6 +278,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const float* o, const 
   if (static_cast<long long>(B) * Hq * ((Sq + 127) / 128) > (1ll << 30) ||
       static_cast<long long>(B) * Hkv * ((Sk + 127) / 128) > (1ll << 30))
     return ATTN_ERR_UNSUPPORTED;
+  // Delta rows are indexed with int.
+  if (static_cast<long long>(B) * Hq * Sq > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||

@@ -211,3 +211,28 @@ def test_decode_num_splits_rejects(lib):
     assert lib.attn_decode_num_splits(1, 4, 1, 64, None) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_decode_num_splits(0, 4, 1, 64, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_decode_num_splits(1, 6, 4, 64, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
+
+
+def bwdc(lib, B=1, Hq=2, Hkv=1, Sq=64, Sk=64, D=64, causal=0, scale=0.125, q=A):
+    return lib.attn_bwd(q, A, A, A, A, A, A, A, A, A, B, Hq, Hkv, Sq, Sk, D, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=1024, Hq=1024, Sq=1025), attn.ATTN_ERR_UNSUPPORTED),   # > 2^30 Delta rows
+    (dict(q=M), attn.ATTN_ERR_MISALIGNED),
+])
+def test_bwd_rejects(lib, kw, code):
+    assert bwdc(lib, **kw) == code
+
+
+def test_decode_rejects_too_many_rows(lib):
+    # B * Hq above 2^30 output rows
+    # (every other limit holds: B*Hkv*Sk*D and ns*B*Hq*D are small, Hkv*slices <= 65535)
+    assert dec(lib, B=65535, Hq=32768, Hkv=1, Sk=1, D=64, ns=1) == attn.ATTN_ERR_UNSUPPORTED
+    assert dec(lib, B=32768, Hq=32768, Hkv=1, Sk=1, D=64, ns=1, q=None) == attn.ATTN_ERR_INVALID_ARG
