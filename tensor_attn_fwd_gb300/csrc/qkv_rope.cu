@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -491,18 +492,20 @@ cudaError_t launch_qkv_rope(const void* x, const void* w, const float* rope, con
   cfg.blockDim = dim3(kGThreads, 1, 1);
   cfg.dynamicSmemBytes = GCfg<true>::kSmem;
   cfg.stream = stream;
-  static int max_clusters[64] = {0};  // clusters of two resident at once, per device
+  // Clusters of two resident at once, per device (computed once; concurrent
+  // first calls store the same value).
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_clusters[dev] == 0) {
+  int resident = max_clusters[dev].load(std::memory_order_relaxed);
+  if (resident == 0) {
     cfg.gridDim = dim3(2, 1, 1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0)
-      n = sm_count() / 2;
-    max_clusters[dev] = n;
+    if (cudaOccupancyMaxActiveClusters(&resident, kernel, &cfg) != cudaSuccess || resident <= 0)
+      resident = sm_count() / 2;
+    max_clusters[dev].store(resident, std::memory_order_relaxed);
   }
   const int total = p.mt * p.nt;
-  const int clusters = total < max_clusters[dev] ? total : max_clusters[dev];
+  const int clusters = total < resident ? total : resident;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   e = cudaLaunchKernelEx(&cfg, qkv_rope_kernel<true>, tmX, tmW, p);
   if (e != cudaSuccess) return e;
