@@ -13,7 +13,8 @@
 // Roles (384 threads):
 //   warps 0-3  softmax for query tile 0  (thread r owns TMEM lane / row r)
 //   warps 4-7  softmax for query tile 1
-//   warp  8    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warp  8    MMA issuer (whole warp, one elected lane issues): S_t = Q_t K_j^T
+//              and O_t += P_t V_j
 //   warp  9    TMA producer (one thread): Q tiles and a K/V stage ring
 //   warps 10-11 idle
 //
@@ -157,6 +158,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
+// The same wait for a whole converged warp; the vote keeps the lanes together
+// and the outcome uniform.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* bars) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, bars));
+}
+
 // ------------------------------------------------------------------ producer
 template <int D>
 __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
@@ -240,9 +247,9 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
       const uint64_t a = desc_from_words(a0 + off, kHi);
       const uint64_t b = desc_from_words(b0 + off, kHi);
       if (kk == 0)
-        mma_ss_c<0>(d, a, b, C::kIdescQK);
+        mma_ss_w<0>(d, a, b, C::kIdescQK);
       else
-        mma_ss_c<1>(d, a, b, C::kIdescQK);
+        mma_ss_w<1>(d, a, b, C::kIdescQK);
     }
   };
   // O_t (+)= P_t V for key steps [kk0, kk0+4) (P from TMEM, V MN-major).
@@ -255,14 +262,14 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
       const int kk = half * 4 + k4;
       const uint64_t bd = desc_from_words(b0 + kk * (2048 >> 4), kHi);
       if (first && kk == 0)
-        mma_ts_c<0>(d, a + kk * 8, bd, C::kIdescPV);
+        mma_ts_w<0>(d, a + kk * 8, bd, C::kIdescPV);
       else
-        mma_ts_c<1>(d, a + kk * 8, bd, C::kIdescPV);
+        mma_ts_w<1>(d, a + kk * 8, bd, C::kIdescPV);
     }
   };
   auto acquire_kv = [&](uint32_t& st) -> bool {
     st = kv_ctr % C::kStages;
-    if (!wait_or_abort(&bars->kv_full[st], (kv_ctr / C::kStages) & 1, bars)) return false;
+    if (!wait_warp(&bars->kv_full[st], (kv_ctr / C::kStages) & 1, bars)) return false;
     ++kv_ctr;
     return true;
   };
@@ -273,15 +280,15 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
     const Item it = get_item(p, idx);
     const int n = max(it.n[0], it.n[1]);
     if (n == 0) continue;
-    if (!(ok = wait_or_abort(&bars->q_full, q_ctr & 1, bars))) break;
+    if (!(ok = wait_warp(&bars->q_full, q_ctr & 1, bars))) break;
     ++q_ctr;
 
     // Q may be overwritten once the item's last S MMA has completed.
     int s_left = it.n[0] + it.n[1];
     auto issue_s_counted = [&](int t, uint32_t st) {
       issue_s(t, st);
-      tc_commit(&bars->s_full[t]);
-      if (--s_left == 0) tc_commit(&bars->q_empty);
+      tc_commit_w(&bars->s_full[t]);
+      if (--s_left == 0) tc_commit_w(&bars->q_empty);
     };
     uint32_t kst;
     if (!(ok = acquire_kv(kst))) break;
@@ -290,7 +297,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
     for (int t = 0; t < 2; ++t) {
       if (it.n[t] > 0) issue_s_counted(t, kst);
     }
-    tc_commit(&bars->kv_empty[kst]);
+    tc_commit_w(&bars->kv_empty[kst]);
 
     for (int j = 0; j < n && ok; ++j) {
       // Both operand tiles of this step are acquired before any P wait, so
@@ -306,26 +313,26 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
         // while the softmax warps are still producing the second.
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          if (!(ok = wait_or_abort(&bars->p_full[t][half], p_phase[t], bars))) break;
+          if (!(ok = wait_warp(&bars->p_full[t][half], p_phase[t], bars))) break;
           tc_fence_after();
           issue_pv_half(t, vst, half, j == 0);
         }
         if (!ok) break;
         p_phase[t] ^= 1;
         if (j == it.n[t] - 1)
-          tc_commit(&bars->o_full[t]);
+          tc_commit_w(&bars->o_full[t]);
         else
           issue_s_counted(t, nkst);
       }
       if (!ok) break;
-      tc_commit(&bars->kv_empty[vst]);
-      if (has_next) tc_commit(&bars->kv_empty[nkst]);
+      tc_commit_w(&bars->kv_empty[vst]);
+      if (has_next) tc_commit_w(&bars->kv_empty[nkst]);
     }
     if (!ok) break;
   }
   if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
   // Every MMA this thread issued must finish before TMEM is released.
-  tc_commit(&bars->mma_done);
+  tc_commit_w(&bars->mma_done);
   (void)mbar_wait(&bars->mma_done, 0);
 }
 
@@ -572,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     setmaxnreg_dec<kRegsOther>();
     if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D>(p, sQ, sKV, bars, tmem);
+      mma_role<D>(p, sQ, sKV, bars, tmem);
     } else if (warp == kLoadWarp) {
       if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
     }
