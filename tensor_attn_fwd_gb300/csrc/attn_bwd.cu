@@ -108,6 +108,14 @@ __device__ __forceinline__ void bwd_record(int* status) {
   if (status != nullptr) atomicCAS(status, 0, ATTN_ERR_TIMEOUT);
 }
 
+__device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, BwdBars* bars);
+
+// The wait for a whole converged warp (the TMA and MMA roles run as whole warps
+// and issue from one elected lane); the vote keeps the outcome uniform.
+__device__ __forceinline__ bool bwd_wait_w(uint64_t* bar, uint32_t parity, BwdBars* bars) {
+  return __all_sync(0xffffffffu, bwd_wait(bar, parity, bars));
+}
+
 __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, BwdBars* bars) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
@@ -171,7 +179,7 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
   for (int s = 0; s < D / 64; ++s) tma_load_3d(dst + s * kSub, map, bar, s * 64, row0, plane);
 }
 
-// One 128x128 SS product into TMEM column d_col: a b^T (K-major tiles, D deep).
+// One 128x128 SS product into TMEM column d_col (called by the whole MMA warp): a b^T (K-major tiles, D deep).
 template <int D>
 __device__ __forceinline__ void mma_ss_tile(uint32_t tmem, uint32_t d_col, uint32_t a_smem,
                                             uint32_t b_smem) {
@@ -187,13 +195,14 @@ __device__ __forceinline__ void mma_ss_tile(uint32_t tmem, uint32_t d_col, uint3
     const uint64_t ad = desc_from_words(a + off, kHi);
     const uint64_t bd = desc_from_words(b + off, kHi);
     if (kk == 0)
-      mma_ss_c<0>(tmem + d_col, ad, bd, C::kIdescSS);
+      mma_ss_w<0>(tmem + d_col, ad, bd, C::kIdescSS);
     else
-      mma_ss_c<1>(tmem + d_col, ad, bd, C::kIdescSS);
+      mma_ss_w<1>(tmem + d_col, ad, bd, C::kIdescSS);
   }
 }
 
-// acc (+)= A(tmem, 128 x 128 bf16 at column a_col) x B(smem tile, MN-major).
+// acc (+)= A(tmem, 128 x 128 bf16 at column a_col) x B(smem tile, MN-major)
+// (called by the whole MMA warp).
 template <int D>
 __device__ __forceinline__ void mma_ts_acc(uint32_t tmem, uint32_t acc_col, uint32_t a_col,
                                            uint32_t b_smem, bool first) {
@@ -208,9 +217,9 @@ __device__ __forceinline__ void mma_ts_acc(uint32_t tmem, uint32_t acc_col, uint
     // bf16 A: rows 0-63 packed at columns [0,32), rows 64-127 at [64,96).
     const uint32_t ac = a_col + kk * 8 + (kk >= 4 ? 32 : 0);
     if (first && kk == 0)
-      mma_ts_c<0>(tmem + acc_col, tmem + ac, bd, C::kIdescTS);
+      mma_ts_w<0>(tmem + acc_col, tmem + ac, bd, C::kIdescTS);
     else
-      mma_ts_c<1>(tmem + acc_col, tmem + ac, bd, C::kIdescTS);
+      mma_ts_w<1>(tmem + acc_col, tmem + ac, bd, C::kIdescTS);
   }
 }
 
@@ -288,20 +297,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bool ok = true;
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0 && nsteps > 0) {
-      mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
-      load_tile<D>(sK, &tmK, &bars->fixed_full, 128 * n, bg);
-      load_tile<D>(sV, &tmV, &bars->fixed_full, 128 * n, bg);
+    if (nsteps > 0) {
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
+        load_tile<D>(sK, &tmK, &bars->fixed_full, 128 * n, bg);
+        load_tile<D>(sV, &tmV, &bars->fixed_full, 128 * n, bg);
+      }
+      __syncwarp();
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % kStages;
-        if (s >= kStages && !(ok = bwd_wait(&bars->empty[st], ((s / kStages) - 1) & 1, bars)))
+        if (s >= kStages && !(ok = bwd_wait_w(&bars->empty[st], ((s / kStages) - 1) & 1, bars)))
           break;
         const int h = g * group + s / per_head;
         const int m = m0 + s % per_head;
         uint8_t* dst = sRing + st * 2 * C::kTile;
-        mbar_arrive_expect_tx(&bars->full[st], 2 * C::kTile);
-        load_tile<D>(dst, &tmQ, &bars->full[st], 128 * m, b * p.Hq + h);
-        load_tile<D>(dst + C::kTile, &tmDO, &bars->full[st], 128 * m, b * p.Hq + h);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars->full[st], 2 * C::kTile);
+          load_tile<D>(dst, &tmQ, &bars->full[st], 128 * m, b * p.Hq + h);
+          load_tile<D>(dst + C::kTile, &tmDO, &bars->full[st], 128 * m, b * p.Hq + h);
+        }
+        __syncwarp();
       }
       if (!ok) bwd_record(p.status);
       for (int s = max(0, nsteps - kStages); s < nsteps; ++s)
@@ -309,18 +324,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (void)mbar_wait(&bars->fixed_full, 0);
     }
   } else if (warp == kBwdMmaWarp) {
-    if (lane == 0 && nsteps > 0) {
-      ok = bwd_wait(&bars->fixed_full, 0, bars);
+    if (nsteps > 0) {
+      ok = bwd_wait_w(&bars->fixed_full, 0, bars);
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       // S^T = K Q^T and dP^T = V dO^T of step s (its Q/dO stage must have landed).
       auto issue_sd = [&](int s) -> bool {
         const int st = s % kStages;
-        if (!bwd_wait(&bars->full[st], (s / kStages) & 1, bars)) return false;
+        if (!bwd_wait_w(&bars->full[st], (s / kStages) & 1, bars)) return false;
         const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
         mma_ss_tile<D>(tmem, C::kColS, k_addr, q_addr);
-        tc_commit(&bars->s_full);
+        tc_commit_w(&bars->s_full);
         mma_ss_tile<D>(tmem, C::kColDP, v_addr, q_addr + C::kTile);
-        tc_commit(&bars->dp_full);
+        tc_commit_w(&bars->dp_full);
         return true;
       };
       if (ok) ok = issue_sd(0);
@@ -330,21 +345,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t do_addr = q_addr + C::kTile;
         // dV += P^T dO as soon as P^T is in TMEM (B operands MN-major: their
         // rows are the K dimension) ...
-        if (!(ok = bwd_wait(&bars->p_ready, s & 1, bars))) break;
+        if (!(ok = bwd_wait_w(&bars->p_ready, s & 1, bars))) break;
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA1, C::kColS, do_addr, s == 0);
         // ... dK += dS^T Q once dS^T is; then the stage is free.
-        if (!(ok = bwd_wait(&bars->ds_full, s & 1, bars))) break;
+        if (!(ok = bwd_wait_w(&bars->ds_full, s & 1, bars))) break;
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, q_addr, s == 0);
-        tc_commit(&bars->empty[st]);
+        tc_commit_w(&bars->empty[st]);
         // The next step's S^T / dP^T overwrite P^T / dS^T only after the two
         // products above have read them (same-thread tcgen05 order).
         if (s + 1 < nsteps && !(ok = issue_sd(s + 1))) break;
       }
-      if (ok) tc_commit(&bars->acc_full);
+      if (ok) tc_commit_w(&bars->acc_full);
       if (!ok) bwd_record(p.status);
-      tc_commit(&bars->mma_done);
+      tc_commit_w(&bars->mma_done);
       (void)mbar_wait(&bars->mma_done, 0);
     }
   } else {
@@ -543,23 +558,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bool ok = true;
 
   if (warp == kBwdLoadWarp) {
-    if (lane == 0 && nsteps > 0) {
-      mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
-      load_tile<D>(sQ, &tmQ, &bars->fixed_full, 128 * m, bh);
-      load_tile<D>(sDO, &tmDO, &bars->fixed_full, 128 * m, bh);
+    if (nsteps > 0) {
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
+        load_tile<D>(sQ, &tmQ, &bars->fixed_full, 128 * m, bh);
+        load_tile<D>(sDO, &tmDO, &bars->fixed_full, 128 * m, bh);
+      }
+      __syncwarp();
       // K(s) and V(s) in use order; K(s) is held until dQ(s), V(s) until dP(s).
       for (int s = 0; s < nsteps && ok; ++s) {
         const int sk = s % kKStages, sv = s % kVStages;
         if (s >= kKStages &&
-            !(ok = bwd_wait(&bars->empty[sk], ((s / kKStages) - 1) & 1, bars)))
+            !(ok = bwd_wait_w(&bars->empty[sk], ((s / kKStages) - 1) & 1, bars)))
           break;
-        mbar_arrive_expect_tx(&bars->full[sk], C::kTile);
-        load_tile<D>(sK + sk * C::kTile, &tmK, &bars->full[sk], 128 * s, bkv);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars->full[sk], C::kTile);
+          load_tile<D>(sK + sk * C::kTile, &tmK, &bars->full[sk], 128 * s, bkv);
+        }
+        __syncwarp();
         if (s >= kVStages &&
-            !(ok = bwd_wait(&bars->empty_v[sv], ((s / kVStages) - 1) & 1, bars)))
+            !(ok = bwd_wait_w(&bars->empty_v[sv], ((s / kVStages) - 1) & 1, bars)))
           break;
-        mbar_arrive_expect_tx(&bars->full_v[sv], C::kTile);
-        load_tile<D>(sV + sv * C::kTile, &tmV, &bars->full_v[sv], 128 * s, bkv);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars->full_v[sv], C::kTile);
+          load_tile<D>(sV + sv * C::kTile, &tmV, &bars->full_v[sv], 128 * s, bkv);
+        }
+        __syncwarp();
       }
       if (!ok) bwd_record(p.status);
       for (int s = max(0, nsteps - kKStages); s < nsteps; ++s)
@@ -569,44 +593,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (void)mbar_wait(&bars->fixed_full, 0);
     }
   } else if (warp == kBwdMmaWarp) {
-    if (lane == 0 && nsteps > 0) {
-      ok = bwd_wait(&bars->fixed_full, 0, bars);
+    if (nsteps > 0) {
+      ok = bwd_wait_w(&bars->fixed_full, 0, bars);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
       auto issue_s = [&](int s) -> bool {  // S = Q K^T
         const int sk = s % kKStages;
-        if (!bwd_wait(&bars->full[sk], (s / kKStages) & 1, bars)) return false;
+        if (!bwd_wait_w(&bars->full[sk], (s / kKStages) & 1, bars)) return false;
         mma_ss_tile<D>(tmem, C::kColS, q_addr, k_base + sk * C::kTile);
-        tc_commit(&bars->s_full);
+        tc_commit_w(&bars->s_full);
         return true;
       };
       auto issue_dp = [&](int s) -> bool {  // dP = dO V^T; V(s) is free afterwards
         const int sv = s % kVStages;
-        if (!bwd_wait(&bars->full_v[sv], (s / kVStages) & 1, bars)) return false;
+        if (!bwd_wait_w(&bars->full_v[sv], (s / kVStages) & 1, bars)) return false;
         mma_ss_tile<D>(tmem, C::kColDP, do_addr, v_base + sv * C::kTile);
-        tc_commit(&bars->dp_full);
-        tc_commit(&bars->empty_v[sv]);
+        tc_commit_w(&bars->dp_full);
+        tc_commit_w(&bars->empty_v[sv]);
         return true;
       };
       if (ok) ok = issue_s(0) && issue_dp(0);
       for (int s = 0; s < nsteps && ok; ++s) {
         // S(s+1) as soon as the gradient warps have read S(s) ...
         if (s + 1 < nsteps) {
-          if (!(ok = bwd_wait(&bars->p_ready, s & 1, bars))) break;
+          if (!(ok = bwd_wait_w(&bars->p_ready, s & 1, bars))) break;
           tc_fence_after();
           if (!(ok = issue_s(s + 1))) break;
         }
         // ... dQ += dS K once dS(s) is in TMEM (K MN-major: its rows are the K dim) ...
-        if (!(ok = bwd_wait(&bars->ds_full, s & 1, bars))) break;
+        if (!(ok = bwd_wait_w(&bars->ds_full, s & 1, bars))) break;
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, k_base + (s % kKStages) * C::kTile, s == 0);
-        tc_commit(&bars->empty[s % kKStages]);
+        tc_commit_w(&bars->empty[s % kKStages]);
         // ... then dP(s+1), which overwrites dS(s) after dQ has read it.
         if (s + 1 < nsteps && !(ok = issue_dp(s + 1))) break;
       }
-      if (ok) tc_commit(&bars->acc_full);
+      if (ok) tc_commit_w(&bars->acc_full);
       if (!ok) bwd_record(p.status);
-      tc_commit(&bars->mma_done);
+      tc_commit_w(&bars->mma_done);
       (void)mbar_wait(&bars->mma_done, 0);
     }
   } else {

@@ -15,7 +15,8 @@
 //   warps 4-7  softmax for query tile 1
 //   warp  8    MMA issuer (whole warp, one elected lane issues): S_t = Q_t K_j^T
 //              and O_t += P_t V_j
-//   warp  9    TMA producer (one thread): Q tiles and a K/V stage ring
+//   warp  9    TMA producer (whole warp, one elected lane issues): Q tiles and a
+//              K/V stage ring
 //   warps 10-11 idle
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
@@ -180,28 +181,34 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     if (n == 0) continue;
     const int b = it.bh / p.Hq, h = it.bh % p.Hq;
     const int bkv = b * p.Hkv + h / group;
-    if (q_ctr > 0 && !(ok = wait_or_abort(&bars->q_empty, (q_ctr - 1) & 1, bars))) break;
-    mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
+    if (q_ctr > 0 && !(ok = wait_warp(&bars->q_empty, (q_ctr - 1) & 1, bars))) break;
+    if (elect_one()) {
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
+      for (int t = 0; t < 2; ++t)
 #pragma unroll
-      for (int s = 0; s < C::kSub; ++s)
-        tma_load_3d(sQ + t * C::kTileBytes + s * kSubBytes, tmQ, &bars->q_full, s * 64,
-                    it.q_row0 + 128 * t, it.bh);
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sQ + t * C::kTileBytes + s * kSubBytes, tmQ, &bars->q_full, s * 64,
+                      it.q_row0 + 128 * t, it.bh);
+    }
+    __syncwarp();
     ++q_ctr;
     for (int j = 0; j < n && ok; ++j) {
 #pragma unroll 1
       for (int kind = 0; kind < 2; ++kind) {
         const uint32_t st = kv_ctr % C::kStages;
         if (kv_ctr >= uint32_t(C::kStages) &&
-            !(ok = wait_or_abort(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars)))
+            !(ok = wait_warp(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars)))
           break;
-        mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
-        const CUtensorMap* map = kind ? tmV : tmK;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
+          const CUtensorMap* map = kind ? tmV : tmK;
 #pragma unroll
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, map, &bars->kv_full[st], s * 64,
-                      j * 128, bkv);
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, map, &bars->kv_full[st],
+                        s * 64, j * 128, bkv);
+        }
+        __syncwarp();
         ++kv_ctr;
       }
     }
@@ -581,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) {
       mma_role<D>(p, sQ, sKV, bars, tmem);
     } else if (warp == kLoadWarp) {
-      if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+      load_role<D>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
     }
   }
 

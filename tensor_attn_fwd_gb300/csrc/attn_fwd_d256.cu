@@ -22,7 +22,8 @@
 // the 64 KB Q tile.
 //
 // Roles (192 threads): warps 0-3 softmax (thread r owns row / TMEM lane r) and
-// epilogue, warp 4 MMA issue (one thread), warp 5 TMA (one thread).
+// epilogue, warp 4 MMA issue, warp 5 TMA (each a whole warp; one elected lane
+// issues).
 //
 // O rescale hazard: S(g) completes before O += P(g-1) V(g-1) has run, so a
 // softmax thread that must rescale O at step g first waits for that product.
@@ -147,6 +148,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars256
   }
 }
 
+// The same wait for a whole converged warp (the TMA and MMA roles run as whole
+// warps and issue from one elected lane); the vote keeps the outcome uniform.
+__device__ __forceinline__ bool wait_bar_w(uint64_t* bar, uint32_t parity, Bars256* bars) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, bars));
+}
+
 // ------------------------------------------------------------------ producer
 // Load order (= the MMA warp's use order):
 //   Q(i0) K_0(i0) | K_1 V_0 | K_2 V_1 | ... | K_{n-1} V_{n-2} | Q(i1) K_0(i1) V_{n-1} | ...
@@ -159,13 +166,16 @@ __device__ __forceinline__ bool load_half(const CUtensorMap* map, int half, int 
                                           uint8_t* sKV, Bars256* bars, Ring& ring) {
   const uint32_t st = ring.ctr % kStages256;
   if (ring.ctr >= uint32_t(kStages256) &&
-      !wait_bar(&bars->kv_empty[st], ((ring.ctr / kStages256) - 1) & 1, bars))
+      !wait_bar_w(&bars->kv_empty[st], ((ring.ctr / kStages256) - 1) & 1, bars))
     return false;
-  mbar_arrive_expect_tx(&bars->kv_full[st], kHalfBytes);
+  if (elect_one()) {
+    mbar_arrive_expect_tx(&bars->kv_full[st], kHalfBytes);
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
-    tma_load_3d(sKV + st * kHalfBytes + s * kSub, map, &bars->kv_full[st], half * 128 + s * 64,
-                key0, plane);
+    for (int s = 0; s < 2; ++s)
+      tma_load_3d(sKV + st * kHalfBytes + s * kSub, map, &bars->kv_full[st],
+                  half * 128 + s * 64, key0, plane);
+  }
+  __syncwarp();
   ++ring.ctr;
   return true;
 }
@@ -181,11 +191,14 @@ __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   Item256 it;
   if (!next_work(p, r, it)) return;
   auto load_q_k0 = [&](const Item256& x) -> bool {
-    if (q_ctr > 0 && !wait_bar(&bars->q_empty, (q_ctr - 1) & 1, bars)) return false;
-    mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+    if (q_ctr > 0 && !wait_bar_w(&bars->q_empty, (q_ctr - 1) & 1, bars)) return false;
+    if (elect_one()) {
+      mbar_arrive_expect_tx(&bars->q_full, kQBytes);
 #pragma unroll
-    for (int s = 0; s < 4; ++s)
-      tma_load_3d(sQ + s * kSub, tmQ, &bars->q_full, s * 64, x.row0, x.bh);
+      for (int s = 0; s < 4; ++s)
+        tma_load_3d(sQ + s * kSub, tmQ, &bars->q_full, s * 64, x.row0, x.bh);
+    }
+    __syncwarp();
     ++q_ctr;
     const int bkv = (x.bh / p.Hq) * p.Hkv + (x.bh % p.Hq) / group;
     return load_half(tmK, 0, 0, bkv, sKV, bars, ring) && load_half(tmK, 1, 0, bkv, sKV, bars, ring);
@@ -237,7 +250,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
 
   auto acquire = [&](uint32_t& st) -> bool {
     st = kv_ctr % kStages256;
-    if (!wait_bar(&bars->kv_full[st], (kv_ctr / kStages256) & 1, bars)) return false;
+    if (!wait_bar_w(&bars->kv_full[st], (kv_ctr / kStages256) & 1, bars)) return false;
     ++kv_ctr;
     return true;
   };
@@ -255,13 +268,13 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
       const uint64_t a = desc_from_words(q_lo + qoff, kHi);
       const uint64_t b = desc_from_words(k_lo + koff, kHi);
       if (kk == 0)
-        mma_ss_c<0>(d, a, b, kIdescQK256);
+        mma_ss_w<0>(d, a, b, kIdescQK256);
       else
-        mma_ss_c<1>(d, a, b, kIdescQK256);
+        mma_ss_w<1>(d, a, b, kIdescQK256);
     }
-    tc_commit(&bars->s_full[g_s & 1]);
-    tc_commit(&bars->kv_empty[st0]);
-    tc_commit(&bars->kv_empty[st1]);
+    tc_commit_w(&bars->s_full[g_s & 1]);
+    tc_commit_w(&bars->kv_empty[st0]);
+    tc_commit_w(&bars->kv_empty[st1]);
     ++g_s;
     return true;
   };
@@ -269,10 +282,10 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
   int r = 0;
   Item256 it;
   if (!next_work(p, r, it)) return;
-  if (!(ok = wait_bar(&bars->q_full, q_ctr & 1, bars))) goto done;
+  if (!(ok = wait_bar_w(&bars->q_full, q_ctr & 1, bars))) goto done;
   ++q_ctr;
   if (!(ok = issue_s())) goto done;
-  if (it.n == 1) tc_commit(&bars->q_empty);
+  if (it.n == 1) tc_commit_w(&bars->q_empty);
   while (true) {
     Item256 nxt;
     bool have_next = false;
@@ -280,14 +293,14 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
       // Scores of the next step first: this item's tile j+1, or the next item's tile 0.
       if (j + 1 < it.n) {
         if (!(ok = issue_s())) goto done;
-        if (j + 2 == it.n) tc_commit(&bars->q_empty);  // the item's last S is issued
+        if (j + 2 == it.n) tc_commit_w(&bars->q_empty);  // the item's last S is issued
       } else {
         have_next = next_work(p, r, nxt);
         if (have_next) {
-          if (!(ok = wait_bar(&bars->q_full, q_ctr & 1, bars))) goto done;
+          if (!(ok = wait_bar_w(&bars->q_full, q_ctr & 1, bars))) goto done;
           ++q_ctr;
           if (!(ok = issue_s())) goto done;
-          if (nxt.n == 1) tc_commit(&bars->q_empty);
+          if (nxt.n == 1) tc_commit_w(&bars->q_empty);
         }
       }
       // O += P(g) V(g), in two key halves as P arrives.
@@ -298,7 +311,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
       const uint32_t par = (g_pv >> 1) & 1;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        if (!(ok = wait_bar(&bars->p_full[buf][half], par, bars))) goto done;
+        if (!(ok = wait_bar_w(&bars->p_full[buf][half], par, bars))) goto done;
         tc_fence_after();
 #pragma unroll
         for (int vh = 0; vh < 2; ++vh) {
@@ -309,15 +322,15 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
             const int kk = half * 4 + k4;
             const uint64_t bd = desc_from_words(b0 + kk * (2048 >> 4), kHi);
             if (j == 0 && kk == 0)
-              mma_ts_c<0>(d, a + kk * 8, bd, kIdescPV256);
+              mma_ts_w<0>(d, a + kk * 8, bd, kIdescPV256);
             else
-              mma_ts_c<1>(d, a + kk * 8, bd, kIdescPV256);
+              mma_ts_w<1>(d, a + kk * 8, bd, kIdescPV256);
           }
         }
       }
-      tc_commit(&bars->pv_done[g_pv & 1]);
-      tc_commit(&bars->kv_empty[v0]);
-      tc_commit(&bars->kv_empty[v1]);
+      tc_commit_w(&bars->pv_done[g_pv & 1]);
+      tc_commit_w(&bars->kv_empty[v0]);
+      tc_commit_w(&bars->kv_empty[v1]);
       ++g_pv;
     }
     if (!have_next) break;
@@ -326,7 +339,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
 done:
   if (!ok) note_status(p.status, ATTN_ERR_TIMEOUT);
   // Every MMA this thread issued must finish before TMEM is released.
-  tc_commit(&bars->mma_done);
+  tc_commit_w(&bars->mma_done);
   (void)mbar_wait(&bars->mma_done, 0);
 }
 
@@ -561,9 +574,9 @@ __global__ void __launch_bounds__(kThreads256, 1)
   if (warp < 4) {
     softmax_role256(p, bars, tmem, warp, lane);
   } else if (warp == kMmaWarp256) {
-    if (lane == 0) mma_role256(p, sQ, sKV, bars, tmem);
+    mma_role256(p, sQ, sKV, bars, tmem);
   } else if (warp == kLoadWarp256) {
-    if (lane == 0) load_role256(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+    load_role256(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
   }
 
   tc_fence_before();

@@ -239,6 +239,17 @@ __device__ __forceinline__ void mma_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint6
 // when the whole warp runs it, so the MMA issuers are whole warps.  With the
 // full mask and a converged warp the elected lane is the same every time, so
 // a commit tracks every MMA the warp issued.  All 32 lanes must call these.
+// True in exactly one lane of the converged warp (the lowest).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, e;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 template <uint32_t ACC>
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc) {
@@ -524,6 +535,30 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar_local, uint16_t m
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(bar_local),
+      "h"(mask)
+      : "memory");
+}
+
+// The pair MMA and the multicast commit issued from a converged warp (one
+// elected lane; all 32 lanes must call them).
+template <uint32_t ACC>
+__device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_mc_w(uint32_t bar_local, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}\n" ::"r"(bar_local),
       "h"(mask)
       : "memory");
 }

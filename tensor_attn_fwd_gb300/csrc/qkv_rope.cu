@@ -27,7 +27,8 @@
 //           the even CTA and count both CTAs' copies; MMA completions are
 //           multicast to both CTAs; both CTAs' epilogue threads release an
 //           accumulator buffer on the even CTA's barrier.
-// Roles (192 threads): warp 0 TMA (one thread), warp 1 MMA (one thread),
+// Roles (192 threads): warp 0 TMA, warp 1 MMA (each a whole warp; one elected
+// lane issues),
 // warps 2-5 epilogue (thread = token row = TMEM lane): tcgen05.ld of the
 // accumulator, rotation with a (cos, sin) table, bf16 rounding, store into
 // Q / K / V.  Rows past T, and features past N, are loaded as zeros by TMA and
@@ -114,6 +115,13 @@ __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, GBars* bar
   }
 }
 
+// The wait for a whole converged warp (the TMA and MMA roles run as whole warps
+// and issue from one elected lane); the vote keeps the outcome uniform.
+template <bool kPair>
+__device__ __forceinline__ bool gwait_w(uint64_t* bar, uint32_t parity, GBars* bars) {
+  return __all_sync(0xffffffffu, gwait<kPair>(bar, parity, bars));
+}
+
 // Work slots: one per CTA (single) or one per CTA pair.
 template <bool kPair>
 __device__ __forceinline__ int g_slot() {
@@ -138,29 +146,32 @@ __device__ void g_load(const CUtensorMap* tmX, const CUtensorMap* tmW, const Qkv
     for (int kb = 0; kb < p.kb; ++kb) {
       const uint32_t st = ctr % C::kStages;
       if (ctr >= uint32_t(C::kStages) &&
-          !(ok = gwait<kPair>(&bars->empty[st], ((ctr / C::kStages) - 1) & 1, bars)))
+          !(ok = gwait_w<kPair>(&bars->empty[st], ((ctr / C::kStages) - 1) & 1, bars)))
         break;
       uint8_t* sA = ring + st * C::kStageBytes;
       // Boxes past `hidden` are zero-filled by TMA and still deliver their bytes.
-      if constexpr (kPair) {
-        // The even CTA's barrier counts both CTAs' bytes.
-        if (rank == 0) mbar_arrive_expect_tx(&bars->full[st], 2 * C::kStageBytes);
-        const uint32_t fb = mapa_shared(smem_u32(&bars->full[st]), 0);
+      if (elect_one()) {
+        if constexpr (kPair) {
+          // The even CTA's barrier counts both CTAs' bytes.
+          if (rank == 0) mbar_arrive_expect_tx(&bars->full[st], 2 * C::kStageBytes);
+          const uint32_t fb = mapa_shared(smem_u32(&bars->full[st]), 0);
 #pragma unroll
-        for (int sub = 0; sub < C::kSubK; ++sub) {
-          const int x = kb * C::kStageK + sub * kBK;
-          tma_load_3d_pair(sA + sub * kASub, tmX, fb, x, m0, 0);
-          tma_load_3d_pair(sA + C::kABytes + sub * C::kBSub, tmW, fb, x, n0, 0);
-        }
-      } else {
-        mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
+          for (int sub = 0; sub < C::kSubK; ++sub) {
+            const int x = kb * C::kStageK + sub * kBK;
+            tma_load_3d_pair(sA + sub * kASub, tmX, fb, x, m0, 0);
+            tma_load_3d_pair(sA + C::kABytes + sub * C::kBSub, tmW, fb, x, n0, 0);
+          }
+        } else {
+          mbar_arrive_expect_tx(&bars->full[st], C::kStageBytes);
 #pragma unroll
-        for (int sub = 0; sub < C::kSubK; ++sub) {
-          const int x = kb * C::kStageK + sub * kBK;
-          tma_load_3d(sA + sub * kASub, tmX, &bars->full[st], x, m0, 0);
-          tma_load_3d(sA + C::kABytes + sub * C::kBSub, tmW, &bars->full[st], x, n0, 0);
+          for (int sub = 0; sub < C::kSubK; ++sub) {
+            const int x = kb * C::kStageK + sub * kBK;
+            tma_load_3d(sA + sub * kASub, tmX, &bars->full[st], x, m0, 0);
+            tma_load_3d(sA + C::kABytes + sub * C::kBSub, tmW, &bars->full[st], x, n0, 0);
+          }
         }
       }
+      __syncwarp();
       ++ctr;
     }
   }
@@ -181,21 +192,21 @@ __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t t
   const uint32_t lo0 = static_cast<uint32_t>(kDesc) + (smem_u32(ring) >> 4);
   auto commit = [&](uint64_t* bar) {  // completion to both CTAs of a pair
     if constexpr (kPair)
-      tc_commit_pair_mc(smem_u32(bar), 0x3);
+      tc_commit_pair_mc_w(smem_u32(bar), 0x3);
     else
-      tc_commit(bar);
+      tc_commit_w(bar);
   };
   uint32_t ctr = 0, i = 0;
   bool ok = true;
   const int total = p.mt * p.nt;
   for (int t = g_slot<kPair>(); t < total && ok; t += g_slots<kPair>(), ++i) {
     const uint32_t a = i & 1;
-    if (i >= 2 && !(ok = gwait<kPair>(&bars->acc_empty[a], ((i >> 1) - 1) & 1, bars))) break;
+    if (i >= 2 && !(ok = gwait_w<kPair>(&bars->acc_empty[a], ((i >> 1) - 1) & 1, bars))) break;
     tc_fence_after();
     const uint32_t d = tmem + a * kBN;
     for (int kb = 0; kb < p.kb; ++kb) {
       const uint32_t st = ctr % C::kStages;
-      if (!(ok = gwait<kPair>(&bars->full[st], (ctr / C::kStages) & 1, bars))) break;
+      if (!(ok = gwait_w<kPair>(&bars->full[st], (ctr / C::kStages) & 1, bars))) break;
       tc_fence_after();
       const uint32_t sa = lo0 + ((st * C::kStageBytes) >> 4);
       const uint32_t sb = sa + (C::kABytes >> 4);
@@ -206,14 +217,14 @@ __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t t
         const uint64_t bd = desc_from_words(sb + ((sub * C::kBSub + (kk & 3) * 32) >> 4), kHi);
         if constexpr (kPair) {
           if (kb == 0 && kk == 0)
-            mma_ss_pair<0>(d, ad, bd, C::kIdesc);
+            mma_ss_pair_w<0>(d, ad, bd, C::kIdesc);
           else
-            mma_ss_pair<1>(d, ad, bd, C::kIdesc);
+            mma_ss_pair_w<1>(d, ad, bd, C::kIdesc);
         } else {
           if (kb == 0 && kk == 0)
-            mma_ss_c<0>(d, ad, bd, C::kIdesc);
+            mma_ss_w<0>(d, ad, bd, C::kIdesc);
           else
-            mma_ss_c<1>(d, ad, bd, C::kIdesc);
+            mma_ss_w<1>(d, ad, bd, C::kIdesc);
         }
       }
       commit(&bars->empty[st]);
@@ -224,9 +235,9 @@ __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t t
   }
   if (!ok) gnote(p.status, ATTN_ERR_TIMEOUT);
   if constexpr (kPair)
-    tc_commit_pair_mc(smem_u32(&bars->mma_done), 0x1);
+    tc_commit_pair_mc_w(smem_u32(&bars->mma_done), 0x1);
   else
-    tc_commit(&bars->mma_done);
+    tc_commit_w(&bars->mma_done);
   (void)mbar_wait(&bars->mma_done, 0);
 }
 
@@ -393,9 +404,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   if (warp == 0) {
-    if (lane == 0) g_load<kPair>(&tmX, &tmW, p, ring, bars);
+    g_load<kPair>(&tmX, &tmW, p, ring, bars);
   } else if (warp == 1) {
-    if (lane == 0 && mma_cta) g_mma<kPair>(p, ring, bars, tmem);
+    if (mma_cta) g_mma<kPair>(p, ring, bars, tmem);
   } else {
     g_epilogue<kPair>(p, bars, tmem, warp, lane);
   }
