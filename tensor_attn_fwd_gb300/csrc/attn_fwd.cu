@@ -160,10 +160,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 }
 
 // The same wait for a whole converged warp; the vote keeps the lanes together
-// and the outcome uniform.
+// and the outcome uniform.  Used where a wait happens once per work item.
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* bars) {
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, bars));
 }
+// Inside a KV step the TMA and MMA warps wait without a vote (a vote after
+// every wait costs ~5 % of the step): each lane keeps its own outcome, the warp
+// carries on issuing with in-bounds addresses whatever it is, and one vote per
+// step makes the decision to stop uniform.  A lane that is still polling is
+// waited for by the next elect.sync, so the warp reconverges by itself.
 
 // ------------------------------------------------------------------ producer
 template <int D>
@@ -194,12 +199,12 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     __syncwarp();
     ++q_ctr;
     for (int j = 0; j < n && ok; ++j) {
+      bool good = true;
 #pragma unroll 1
       for (int kind = 0; kind < 2; ++kind) {
         const uint32_t st = kv_ctr % C::kStages;
-        if (kv_ctr >= uint32_t(C::kStages) &&
-            !(ok = wait_warp(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars)))
-          break;
+        if (kv_ctr >= uint32_t(C::kStages))
+          good &= wait_or_abort(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars);
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
           const CUtensorMap* map = kind ? tmV : tmK;
@@ -211,6 +216,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
         __syncwarp();
         ++kv_ctr;
       }
+      ok = __all_sync(0xffffffffu, good);
     }
   }
   if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
@@ -274,11 +280,12 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
         mma_ts_w<1>(d, a + kk * 8, bd, C::kIdescPV);
     }
   };
+  // Per-lane outcome (no vote); see the note above wait_warp.
   auto acquire_kv = [&](uint32_t& st) -> bool {
     st = kv_ctr % C::kStages;
-    if (!wait_warp(&bars->kv_full[st], (kv_ctr / C::kStages) & 1, bars)) return false;
+    const bool got = wait_or_abort(&bars->kv_full[st], (kv_ctr / C::kStages) & 1, bars);
     ++kv_ctr;
-    return true;
+    return got;
   };
 
   for (int r = 0; ok; ++r) {
@@ -298,7 +305,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
       if (--s_left == 0) tc_commit_w(&bars->q_empty);
     };
     uint32_t kst;
-    if (!(ok = acquire_kv(kst))) break;
+    if (!(ok = __all_sync(0xffffffffu, acquire_kv(kst)))) break;
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -311,8 +318,8 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
       // their (usually already satisfied) waits overlap queued MMAs.
       uint32_t vst, nkst = 0;
       const bool has_next = j + 1 < n;
-      if (!(ok = acquire_kv(vst))) break;
-      if (has_next && !(ok = acquire_kv(nkst))) break;
+      bool good = acquire_kv(vst);
+      if (has_next) good &= acquire_kv(nkst);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= it.n[t]) continue;
@@ -320,20 +327,19 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
         // while the softmax warps are still producing the second.
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          if (!(ok = wait_warp(&bars->p_full[t][half], p_phase[t], bars))) break;
+          good &= wait_or_abort(&bars->p_full[t][half], p_phase[t], bars);
           tc_fence_after();
           issue_pv_half(t, vst, half, j == 0);
         }
-        if (!ok) break;
         p_phase[t] ^= 1;
         if (j == it.n[t] - 1)
           tc_commit_w(&bars->o_full[t]);
         else
           issue_s_counted(t, nkst);
       }
-      if (!ok) break;
       tc_commit_w(&bars->kv_empty[vst]);
       if (has_next) tc_commit_w(&bars->kv_empty[nkst]);
+      ok = __all_sync(0xffffffffu, good);
     }
     if (!ok) break;
   }
