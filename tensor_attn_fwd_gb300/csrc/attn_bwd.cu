@@ -111,7 +111,11 @@ __device__ __forceinline__ void bwd_record(int* status) {
 __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, BwdBars* bars);
 
 // The wait for a whole converged warp (the TMA and MMA roles run as whole warps
-// and issue from one elected lane); the vote keeps the outcome uniform.
+// and issue from one elected lane); the vote keeps the outcome uniform.  Used
+// once per work item.  Inside a step those warps wait without a vote (a vote
+// per wait costs several per cent): each lane keeps its outcome, issue
+// continues with in-bounds addresses, and one vote per step makes the stop
+// decision uniform; a lane still polling is waited for by the next elect.sync.
 __device__ __forceinline__ bool bwd_wait_w(uint64_t* bar, uint32_t parity, BwdBars* bars) {
   return __all_sync(0xffffffffu, bwd_wait(bar, parity, bars));
 }
@@ -306,8 +310,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % kStages;
-        if (s >= kStages && !(ok = bwd_wait_w(&bars->empty[st], ((s / kStages) - 1) & 1, bars)))
-          break;
+        bool good = true;
+        if (s >= kStages) good = bwd_wait(&bars->empty[st], ((s / kStages) - 1) & 1, bars);
         const int h = g * group + s / per_head;
         const int m = m0 + s % per_head;
         uint8_t* dst = sRing + st * 2 * C::kTile;
@@ -317,6 +321,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           load_tile<D>(dst + C::kTile, &tmDO, &bars->full[st], 128 * m, b * p.Hq + h);
         }
         __syncwarp();
+        ok = __all_sync(0xffffffffu, good);
       }
       if (!ok) bwd_record(p.status);
       for (int s = max(0, nsteps - kStages); s < nsteps; ++s)
@@ -328,34 +333,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = bwd_wait_w(&bars->fixed_full, 0, bars);
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       // S^T = K Q^T and dP^T = V dO^T of step s (its Q/dO stage must have landed).
-      auto issue_sd = [&](int s) -> bool {
+      auto issue_sd = [&](int s) -> bool {  // this lane's wait outcome
         const int st = s % kStages;
-        if (!bwd_wait_w(&bars->full[st], (s / kStages) & 1, bars)) return false;
+        const bool got = bwd_wait(&bars->full[st], (s / kStages) & 1, bars);
         const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
         mma_ss_tile<D>(tmem, C::kColS, k_addr, q_addr);
         tc_commit_w(&bars->s_full);
         mma_ss_tile<D>(tmem, C::kColDP, v_addr, q_addr + C::kTile);
         tc_commit_w(&bars->dp_full);
-        return true;
+        return got;
       };
-      if (ok) ok = issue_sd(0);
+      if (ok) ok = __all_sync(0xffffffffu, issue_sd(0));
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % kStages;
         const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
         const uint32_t do_addr = q_addr + C::kTile;
         // dV += P^T dO as soon as P^T is in TMEM (B operands MN-major: their
         // rows are the K dimension) ...
-        if (!(ok = bwd_wait_w(&bars->p_ready, s & 1, bars))) break;
+        bool good = bwd_wait(&bars->p_ready, s & 1, bars);
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA1, C::kColS, do_addr, s == 0);
         // ... dK += dS^T Q once dS^T is; then the stage is free.
-        if (!(ok = bwd_wait_w(&bars->ds_full, s & 1, bars))) break;
+        good &= bwd_wait(&bars->ds_full, s & 1, bars);
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, q_addr, s == 0);
         tc_commit_w(&bars->empty[st]);
         // The next step's S^T / dP^T overwrite P^T / dS^T only after the two
         // products above have read them (same-thread tcgen05 order).
-        if (s + 1 < nsteps && !(ok = issue_sd(s + 1))) break;
+        if (s + 1 < nsteps) good &= issue_sd(s + 1);
+        ok = __all_sync(0xffffffffu, good);
       }
       if (ok) tc_commit_w(&bars->acc_full);
       if (!ok) bwd_record(p.status);
@@ -568,22 +574,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // K(s) and V(s) in use order; K(s) is held until dQ(s), V(s) until dP(s).
       for (int s = 0; s < nsteps && ok; ++s) {
         const int sk = s % kKStages, sv = s % kVStages;
-        if (s >= kKStages &&
-            !(ok = bwd_wait_w(&bars->empty[sk], ((s / kKStages) - 1) & 1, bars)))
-          break;
+        bool good = true;
+        if (s >= kKStages) good = bwd_wait(&bars->empty[sk], ((s / kKStages) - 1) & 1, bars);
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars->full[sk], C::kTile);
           load_tile<D>(sK + sk * C::kTile, &tmK, &bars->full[sk], 128 * s, bkv);
         }
         __syncwarp();
-        if (s >= kVStages &&
-            !(ok = bwd_wait_w(&bars->empty_v[sv], ((s / kVStages) - 1) & 1, bars)))
-          break;
+        if (s >= kVStages) good &= bwd_wait(&bars->empty_v[sv], ((s / kVStages) - 1) & 1, bars);
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars->full_v[sv], C::kTile);
           load_tile<D>(sV + sv * C::kTile, &tmV, &bars->full_v[sv], 128 * s, bkv);
         }
         __syncwarp();
+        ok = __all_sync(0xffffffffu, good);
       }
       if (!ok) bwd_record(p.status);
       for (int s = max(0, nsteps - kKStages); s < nsteps; ++s)
@@ -597,36 +601,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = bwd_wait_w(&bars->fixed_full, 0, bars);
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-      auto issue_s = [&](int s) -> bool {  // S = Q K^T
+      auto issue_s = [&](int s) -> bool {  // S = Q K^T; this lane's wait outcome
         const int sk = s % kKStages;
-        if (!bwd_wait_w(&bars->full[sk], (s / kKStages) & 1, bars)) return false;
+        const bool got = bwd_wait(&bars->full[sk], (s / kKStages) & 1, bars);
         mma_ss_tile<D>(tmem, C::kColS, q_addr, k_base + sk * C::kTile);
         tc_commit_w(&bars->s_full);
-        return true;
+        return got;
       };
       auto issue_dp = [&](int s) -> bool {  // dP = dO V^T; V(s) is free afterwards
         const int sv = s % kVStages;
-        if (!bwd_wait_w(&bars->full_v[sv], (s / kVStages) & 1, bars)) return false;
+        const bool got = bwd_wait(&bars->full_v[sv], (s / kVStages) & 1, bars);
         mma_ss_tile<D>(tmem, C::kColDP, do_addr, v_base + sv * C::kTile);
         tc_commit_w(&bars->dp_full);
         tc_commit_w(&bars->empty_v[sv]);
-        return true;
+        return got;
       };
-      if (ok) ok = issue_s(0) && issue_dp(0);
+      if (ok) {
+        bool got = issue_s(0);
+        got &= issue_dp(0);
+        ok = __all_sync(0xffffffffu, got);
+      }
       for (int s = 0; s < nsteps && ok; ++s) {
+        bool good = true;
         // S(s+1) as soon as the gradient warps have read S(s) ...
         if (s + 1 < nsteps) {
-          if (!(ok = bwd_wait_w(&bars->p_ready, s & 1, bars))) break;
+          good &= bwd_wait(&bars->p_ready, s & 1, bars);
           tc_fence_after();
-          if (!(ok = issue_s(s + 1))) break;
+          good &= issue_s(s + 1);
         }
         // ... dQ += dS K once dS(s) is in TMEM (K MN-major: its rows are the K dim) ...
-        if (!(ok = bwd_wait_w(&bars->ds_full, s & 1, bars))) break;
+        good &= bwd_wait(&bars->ds_full, s & 1, bars);
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, k_base + (s % kKStages) * C::kTile, s == 0);
         tc_commit_w(&bars->empty[s % kKStages]);
         // ... then dP(s+1), which overwrites dS(s) after dQ has read it.
-        if (s + 1 < nsteps && !(ok = issue_dp(s + 1))) break;
+        if (s + 1 < nsteps) good &= issue_dp(s + 1);
+        ok = __all_sync(0xffffffffu, good);
       }
       if (ok) tc_commit_w(&bars->acc_full);
       if (!ok) bwd_record(p.status);

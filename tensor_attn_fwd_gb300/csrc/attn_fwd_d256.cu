@@ -150,6 +150,10 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Bars256
 
 // The same wait for a whole converged warp (the TMA and MMA roles run as whole
 // warps and issue from one elected lane); the vote keeps the outcome uniform.
+// Used once per work item.  Inside a KV step those warps wait without a vote
+// (a vote per wait costs several per cent): each lane keeps its outcome, issue
+// continues with in-bounds addresses, and one vote per step makes the stop
+// decision uniform; a lane still polling is waited for by the next elect.sync.
 __device__ __forceinline__ bool wait_bar_w(uint64_t* bar, uint32_t parity, Bars256* bars) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, bars));
 }
@@ -165,9 +169,9 @@ struct Ring {
 __device__ __forceinline__ bool load_half(const CUtensorMap* map, int half, int key0, int plane,
                                           uint8_t* sKV, Bars256* bars, Ring& ring) {
   const uint32_t st = ring.ctr % kStages256;
-  if (ring.ctr >= uint32_t(kStages256) &&
-      !wait_bar_w(&bars->kv_empty[st], ((ring.ctr / kStages256) - 1) & 1, bars))
-    return false;
+  bool got = true;
+  if (ring.ctr >= uint32_t(kStages256))
+    got = wait_bar(&bars->kv_empty[st], ((ring.ctr / kStages256) - 1) & 1, bars);
   if (elect_one()) {
     mbar_arrive_expect_tx(&bars->kv_full[st], kHalfBytes);
 #pragma unroll
@@ -177,7 +181,7 @@ __device__ __forceinline__ bool load_half(const CUtensorMap* map, int half, int 
   }
   __syncwarp();
   ++ring.ctr;
-  return true;
+  return got;  // this lane's outcome
 }
 
 __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
@@ -201,7 +205,9 @@ __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     __syncwarp();
     ++q_ctr;
     const int bkv = (x.bh / p.Hq) * p.Hkv + (x.bh % p.Hq) / group;
-    return load_half(tmK, 0, 0, bkv, sKV, bars, ring) && load_half(tmK, 1, 0, bkv, sKV, bars, ring);
+    bool g = load_half(tmK, 0, 0, bkv, sKV, bars, ring);
+    g &= load_half(tmK, 1, 0, bkv, sKV, bars, ring);
+    return __all_sync(0xffffffffu, g);
   };
   ok = load_q_k0(it);
   while (ok) {
@@ -209,16 +215,17 @@ __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     Item256 nxt;
     bool have_next = false;
     for (int j = 0; j < it.n && ok; ++j) {
+      bool g = true;
       if (j + 1 < it.n) {
-        ok = load_half(tmK, 0, (j + 1) * 128, bkv, sKV, bars, ring) &&
-             load_half(tmK, 1, (j + 1) * 128, bkv, sKV, bars, ring);
+        g &= load_half(tmK, 0, (j + 1) * 128, bkv, sKV, bars, ring);
+        g &= load_half(tmK, 1, (j + 1) * 128, bkv, sKV, bars, ring);
       } else {
         have_next = next_work(p, r, nxt);
-        if (have_next) ok = load_q_k0(nxt);
+        if (have_next) g &= load_q_k0(nxt);
       }
-      if (ok)
-        ok = load_half(tmV, 0, j * 128, bkv, sKV, bars, ring) &&
-             load_half(tmV, 1, j * 128, bkv, sKV, bars, ring);
+      g &= load_half(tmV, 0, j * 128, bkv, sKV, bars, ring);
+      g &= load_half(tmV, 1, j * 128, bkv, sKV, bars, ring);
+      ok = __all_sync(0xffffffffu, g);
     }
     if (!ok || !have_next) break;
     it = nxt;
@@ -248,16 +255,18 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
   uint32_t g_s = 0, g_pv = 0;  // steps whose S / PV have been issued
   bool ok = true;
 
+  // Per-lane outcomes (no vote); see the note above wait_bar_w.
   auto acquire = [&](uint32_t& st) -> bool {
     st = kv_ctr % kStages256;
-    if (!wait_bar_w(&bars->kv_full[st], (kv_ctr / kStages256) & 1, bars)) return false;
+    const bool got = wait_bar(&bars->kv_full[st], (kv_ctr / kStages256) & 1, bars);
     ++kv_ctr;
-    return true;
+    return got;
   };
   // S(g) = Q K^T into buffer g % 2; releases the two K halves afterwards.
   auto issue_s = [&]() -> bool {
     uint32_t st0, st1;
-    if (!acquire(st0) || !acquire(st1)) return false;
+    bool got = acquire(st0);
+    got &= acquire(st1);
     tc_fence_after();
     const uint32_t d = tmem + ((g_s & 1) ? kColS1 : kColS0);
 #pragma unroll
@@ -276,7 +285,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
     tc_commit_w(&bars->kv_empty[st0]);
     tc_commit_w(&bars->kv_empty[st1]);
     ++g_s;
-    return true;
+    return got;
   };
 
   int r = 0;
@@ -284,34 +293,36 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
   if (!next_work(p, r, it)) return;
   if (!(ok = wait_bar_w(&bars->q_full, q_ctr & 1, bars))) goto done;
   ++q_ctr;
-  if (!(ok = issue_s())) goto done;
+  if (!(ok = __all_sync(0xffffffffu, issue_s()))) goto done;
   if (it.n == 1) tc_commit_w(&bars->q_empty);
   while (true) {
     Item256 nxt;
     bool have_next = false;
     for (int j = 0; j < it.n; ++j) {
+      bool good = true;
       // Scores of the next step first: this item's tile j+1, or the next item's tile 0.
       if (j + 1 < it.n) {
-        if (!(ok = issue_s())) goto done;
+        good &= issue_s();
         if (j + 2 == it.n) tc_commit_w(&bars->q_empty);  // the item's last S is issued
       } else {
         have_next = next_work(p, r, nxt);
         if (have_next) {
           if (!(ok = wait_bar_w(&bars->q_full, q_ctr & 1, bars))) goto done;
           ++q_ctr;
-          if (!(ok = issue_s())) goto done;
+          good &= issue_s();
           if (nxt.n == 1) tc_commit_w(&bars->q_empty);
         }
       }
       // O += P(g) V(g), in two key halves as P arrives.
       uint32_t v0, v1;
-      if (!(ok = acquire(v0) && acquire(v1))) goto done;
+      good &= acquire(v0);
+      good &= acquire(v1);
       const uint32_t buf = g_pv & 1;
       const uint32_t a = tmem + (buf ? kColS1 : kColS0);
       const uint32_t par = (g_pv >> 1) & 1;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        if (!(ok = wait_bar_w(&bars->p_full[buf][half], par, bars))) goto done;
+        good &= wait_bar(&bars->p_full[buf][half], par, bars);
         tc_fence_after();
 #pragma unroll
         for (int vh = 0; vh < 2; ++vh) {
@@ -332,6 +343,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
       tc_commit_w(&bars->kv_empty[v0]);
       tc_commit_w(&bars->kv_empty[v1]);
       ++g_pv;
+      if (!(ok = __all_sync(0xffffffffu, good))) goto done;
     }
     if (!have_next) break;
     it = nxt;
