@@ -116,7 +116,11 @@ __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, GBars* bar
 }
 
 // The wait for a whole converged warp (the TMA and MMA roles run as whole warps
-// and issue from one elected lane); the vote keeps the outcome uniform.
+// and issue from one elected lane); the vote keeps the outcome uniform.  Used
+// once per output tile.  Per K stage those warps wait without a vote: each lane
+// keeps its outcome, issue continues with in-bounds addresses, and one vote per
+// tile makes the stop decision uniform; a lane still polling is waited for by
+// the next elect.sync.
 template <bool kPair>
 __device__ __forceinline__ bool gwait_w(uint64_t* bar, uint32_t parity, GBars* bars) {
   return __all_sync(0xffffffffu, gwait<kPair>(bar, parity, bars));
@@ -143,11 +147,11 @@ __device__ void g_load(const CUtensorMap* tmX, const CUtensorMap* tmW, const Qkv
   for (int t = g_slot<kPair>(); t < total && ok; t += g_slots<kPair>()) {
     const int m0 = (t / p.nt) * (kPair ? 2 * kBM : kBM) + int(rank) * kBM;
     const int n0 = (t % p.nt) * kBN + int(rank) * int(C::kBRows);
+    bool good = true;
     for (int kb = 0; kb < p.kb; ++kb) {
       const uint32_t st = ctr % C::kStages;
-      if (ctr >= uint32_t(C::kStages) &&
-          !(ok = gwait_w<kPair>(&bars->empty[st], ((ctr / C::kStages) - 1) & 1, bars)))
-        break;
+      if (ctr >= uint32_t(C::kStages))
+        good &= gwait<kPair>(&bars->empty[st], ((ctr / C::kStages) - 1) & 1, bars);
       uint8_t* sA = ring + st * C::kStageBytes;
       // Boxes past `hidden` are zero-filled by TMA and still deliver their bytes.
       if (elect_one()) {
@@ -174,6 +178,7 @@ __device__ void g_load(const CUtensorMap* tmX, const CUtensorMap* tmW, const Qkv
       __syncwarp();
       ++ctr;
     }
+    ok = __all_sync(0xffffffffu, good);
   }
   if (!ok) gnote(p.status, ATTN_ERR_TIMEOUT);
   // Let every copy issued land before the CTA can exit (in the pair form the
@@ -204,9 +209,10 @@ __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t t
     if (i >= 2 && !(ok = gwait_w<kPair>(&bars->acc_empty[a], ((i >> 1) - 1) & 1, bars))) break;
     tc_fence_after();
     const uint32_t d = tmem + a * kBN;
+    bool good = true;
     for (int kb = 0; kb < p.kb; ++kb) {
       const uint32_t st = ctr % C::kStages;
-      if (!(ok = gwait_w<kPair>(&bars->full[st], (ctr / C::kStages) & 1, bars))) break;
+      good &= gwait<kPair>(&bars->full[st], (ctr / C::kStages) & 1, bars);
       tc_fence_after();
       const uint32_t sa = lo0 + ((st * C::kStageBytes) >> 4);
       const uint32_t sb = sa + (C::kABytes >> 4);
@@ -230,7 +236,7 @@ __device__ void g_mma(const QkvParams& p, uint8_t* ring, GBars* bars, uint32_t t
       commit(&bars->empty[st]);
       ++ctr;
     }
-    if (!ok) break;
+    if (!(ok = __all_sync(0xffffffffu, good))) break;
     commit(&bars->acc_full[a]);
   }
   if (!ok) gnote(p.status, ATTN_ERR_TIMEOUT);
