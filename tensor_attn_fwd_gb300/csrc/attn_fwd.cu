@@ -16,7 +16,7 @@
 //   warp  8    MMA issuer (whole warp, one elected lane issues): S_t = Q_t K_j^T
 //              and O_t += P_t V_j
 //   warp  9    TMA producer (whole warp, one elected lane issues): Q tiles and a
-//              K/V stage ring
+//              K/V stage ring; V_j and K_j+1 complete on one barrier
 //   warps 10-11 idle
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
@@ -198,29 +198,63 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     }
     __syncwarp();
     ++q_ctr;
+    // Load order: K_0 alone, then (V_j, K_j+1) as one pair per step, V_n-1 alone.
+    // A pair's two copies complete on V_j's barrier, so the MMA warp waits once
+    // per step for both; K_j+1's own barrier gets a plain arrive, which keeps
+    // every stage at one completed phase per use (a stage alternates between K
+    // and V as the ring wraps).
+    auto take_stage = [&](uint32_t& st) -> bool {
+      st = kv_ctr % C::kStages;
+      bool g = true;
+      if (kv_ctr >= uint32_t(C::kStages))
+        g = wait_or_abort(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars);
+      ++kv_ctr;
+      return g;
+    };
+    {
+      uint32_t st;
+      const bool g = take_stage(st);
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
+#pragma unroll
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[st],
+                      s * 64, 0, bkv);
+      }
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, g);
+    }
     for (int j = 0; j < n && ok; ++j) {
-      bool good = true;
-#pragma unroll 1
-      for (int kind = 0; kind < 2; ++kind) {
-        const uint32_t st = kv_ctr % C::kStages;
-        if (kv_ctr >= uint32_t(C::kStages))
-          good &= wait_or_abort(&bars->kv_empty[st], ((kv_ctr / C::kStages) - 1) & 1, bars);
-        if (elect_one()) {
-          mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
-          const CUtensorMap* map = kind ? tmV : tmK;
+      uint32_t sv, sk = 0;
+      const bool pair = j + 1 < n;
+      bool good = take_stage(sv);
+      if (pair) good &= take_stage(sk);
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars->kv_full[sv], pair ? 2 * C::kTileBytes : C::kTileBytes);
+#pragma unroll
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sKV + sv * C::kTileBytes + s * kSubBytes, tmV, &bars->kv_full[sv],
+                      s * 64, j * 128, bkv);
+        if (pair) {
 #pragma unroll
           for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, map, &bars->kv_full[st],
-                        s * 64, j * 128, bkv);
+            tma_load_3d(sKV + sk * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[sv],
+                        s * 64, (j + 1) * 128, bkv);
+          mbar_arrive(&bars->kv_full[sk]);
         }
-        __syncwarp();
-        ++kv_ctr;
       }
+      __syncwarp();
       ok = __all_sync(0xffffffffu, good);
     }
   }
   if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
-  // Let every copy this thread issued land before the CTA can exit.
+  // Let every copy this thread issued land before the CTA can exit.  Copies of
+  // slots reused since have landed already (their slot was released by the MMA
+  // warp after it saw them).  Each item takes an even number of slots (K_0, then
+  // V/K pairs, then V_n-1) and kStages is odd, so the last kStages uses start
+  // with the first slot of a pair: the barrier that counts a K_j+1 is waited here
+  // whenever K_j+1 is.
+  static_assert(C::kStages % 2 == 1, "drain window must start on a pair's first slot");
   const uint32_t last = kv_ctr;
   for (uint32_t c = (last > uint32_t(C::kStages) ? last - C::kStages : 0); c < last; ++c)
     (void)mbar_wait(&bars->kv_full[c % C::kStages], (c / C::kStages) & 1);
@@ -319,7 +353,10 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
       uint32_t vst, nkst = 0;
       const bool has_next = j + 1 < n;
       bool good = acquire_kv(vst);
-      if (has_next) good &= acquire_kv(nkst);
+      if (has_next) {  // landed with V_j: counted on V_j's barrier
+        nkst = kv_ctr % C::kStages;
+        ++kv_ctr;
+      }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= it.n[t]) continue;
