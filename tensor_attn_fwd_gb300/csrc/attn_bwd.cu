@@ -18,9 +18,10 @@
 //                 and dS^T (bf16, written back into TMEM over S^T / dP^T); then
 //                 dV += P^T dO and dK += dS^T Q accumulate in TMEM.  No atomics.
 //                 Per step the MMA warp issues dV(s) as soon as P^T(s) is in
-//                 TMEM, dK(s) once dS^T(s) is, then S^T(s+1) and dP^T(s+1): the
-//                 gradient warps' exponentials for step s+1 overlap dP^T(s+1),
-//                 and their dS^T overlaps dV, so the tensor core stays busy.
+//                 TMEM and S^T(s+1) right behind it (it overwrites P^T(s) only
+//                 after dV has read it), so the gradient warps' dS^T(s) overlaps
+//                 dV(s) and S^T(s+1); then dK(s) once dS^T(s) is in TMEM and
+//                 dP^T(s+1), which overlap the exponentials of step s+1.
 //   dQ kernel     one CTA per 128-row query tile: S = Q K^T and dP = dO V^T
 //                 recomputed for each visible KV tile, dS written into TMEM,
 //                 dQ += dS K accumulated in TMEM.  S(s+1) is issued as soon as
@@ -332,35 +333,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nsteps > 0) {
       ok = bwd_wait_w(&bars->fixed_full, 0, bars);
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      // S^T = K Q^T and dP^T = V dO^T of step s (its Q/dO stage must have landed).
-      auto issue_sd = [&](int s) -> bool {  // this lane's wait outcome
+      // S^T = K Q^T of step s (its Q/dO stage must have landed) and dP^T = V dO^T.
+      auto issue_s = [&](int s) -> bool {  // this lane's wait outcome
         const int st = s % kStages;
         const bool got = bwd_wait(&bars->full[st], (s / kStages) & 1, bars);
-        const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
-        mma_ss_tile<D>(tmem, C::kColS, k_addr, q_addr);
+        mma_ss_tile<D>(tmem, C::kColS, k_addr, smem_u32(sRing + st * 2 * C::kTile));
         tc_commit_w(&bars->s_full);
-        mma_ss_tile<D>(tmem, C::kColDP, v_addr, q_addr + C::kTile);
-        tc_commit_w(&bars->dp_full);
         return got;
       };
-      if (ok) ok = __all_sync(0xffffffffu, issue_sd(0));
+      auto issue_dp = [&](int s) {  // after issue_s(s), which waited for the stage
+        const int st = s % kStages;
+        mma_ss_tile<D>(tmem, C::kColDP, v_addr, smem_u32(sRing + st * 2 * C::kTile) + C::kTile);
+        tc_commit_w(&bars->dp_full);
+      };
+      if (ok) {
+        const bool got = issue_s(0);
+        issue_dp(0);
+        ok = __all_sync(0xffffffffu, got);
+      }
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % kStages;
         const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
         const uint32_t do_addr = q_addr + C::kTile;
         // dV += P^T dO as soon as P^T is in TMEM (B operands MN-major: their
-        // rows are the K dimension) ...
+        // rows are the K dimension), then at once S^T(s+1): it overwrites P^T(s)
+        // only after dV has read it (same-thread tcgen05 order), and the
+        // gradient warps need S^T(s) no more; they compute dS^T(s) meanwhile.
         bool good = bwd_wait(&bars->p_ready, s & 1, bars);
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA1, C::kColS, do_addr, s == 0);
-        // ... dK += dS^T Q once dS^T is; then the stage is free.
+        if (s + 1 < nsteps) good &= issue_s(s + 1);
+        // dK += dS^T Q once dS^T is in TMEM; then the stage is free, and
+        // dP^T(s+1) may overwrite dS^T(s).
         good &= bwd_wait(&bars->ds_full, s & 1, bars);
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, q_addr, s == 0);
         tc_commit_w(&bars->empty[st]);
-        // The next step's S^T / dP^T overwrite P^T / dS^T only after the two
-        // products above have read them (same-thread tcgen05 order).
-        if (s + 1 < nsteps) good &= issue_sd(s + 1);
+        if (s + 1 < nsteps) issue_dp(s + 1);
         ok = __all_sync(0xffffffffu, good);
       }
       if (ok) tc_commit_w(&bars->acc_full);
@@ -377,10 +386,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int key = 128 * n + r;
     const bool key_valid = key < p.Sk;
-    for (int s = 0; s < nsteps && ok; ++s) {
+    // LSE and Delta of a step's 64 columns (2 per lane), loaded one step ahead:
+    // the loads stay in flight through the previous step's work.  Rows past Sq
+    // load row Sq - 1 (in bounds) and are zeroed when staged.
+    float pre_l[2] = {0.f, 0.f}, pre_d[2] = {0.f, 0.f};
+    auto fetch = [&](int s) {
       const int h = g * group + s / per_head;
       const int m = m0 + s % per_head;
-      const int bh = b * p.Hq + h;
+      const size_t base = static_cast<size_t>(b * p.Hq + h) * p.Sq;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int row = min(128 * m + 64 * half + 32 * u + lane, p.Sq - 1);
+        pre_l[u] = __ldg(p.lse + base + row);
+        pre_d[u] = __ldg(p.delta + base + row);
+      }
+    };
+    if (nsteps > 0) fetch(0);
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int m = m0 + s % per_head;
       // This step's -LSE (log2 domain) and -Delta for the warpgroup's 64
       // columns, in the warp's own buffer (no cross-warp barrier, so an
       // aborting warp cannot strand others); read back as broadcast float4.
@@ -389,14 +412,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();  // every lane is done with the previous step's values
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int t = 64 * half + 32 * u + lane;
-        const int row = 128 * m + t;
-        const bool rv = row < p.Sq;
-        nl2[32 * u + lane] =
-            rv ? -__ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e : 0.f;
-        ndl[32 * u + lane] = rv ? -__ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
+        const bool rv = 128 * m + 64 * half + 32 * u + lane < p.Sq;
+        nl2[32 * u + lane] = rv ? -pre_l[u] * kLog2e : 0.f;
+        ndl[32 * u + lane] = rv ? -pre_d[u] : 0.f;
       }
       __syncwarp();
+      if (s + 1 < nsteps) fetch(s + 1);
       // Visible columns (query rows 128m + col) of this key: [c_lo, c_hi) --
       // row >= key - (Sk - Sq) under the causal mask, row < Sq.
       const int row_lo = p.causal ? key - (p.Sk - p.Sq) : -0x40000000;
