@@ -105,6 +105,13 @@ struct BwdParams {
   float scale, scale_log2;
 };
 
+// Read-only global load issued where it stands in the program.
+__device__ __forceinline__ float ld_nc_f32(const float* ptr) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void bwd_record(int* status) {
   if (status != nullptr) atomicCAS(status, 0, ATTN_ERR_TIMEOUT);
 }
@@ -387,8 +394,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int key = 128 * n + r;
     const bool key_valid = key < p.Sk;
     // LSE and Delta of a step's 64 columns (2 per lane), loaded one step ahead:
-    // the loads stay in flight through the previous step's work.  Rows past Sq
-    // load row Sq - 1 (in bounds) and are zeroed when staged.
+    // the loads stay in flight through the previous step's work (volatile asm
+    // keeps them ahead of that work's tcgen05 operations).  Rows past Sq load
+    // row Sq - 1 (in bounds) and are zeroed when staged.
     float pre_l[2] = {0.f, 0.f}, pre_d[2] = {0.f, 0.f};
     auto fetch = [&](int s) {
       const int h = g * group + s / per_head;
@@ -397,8 +405,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int row = min(128 * m + 64 * half + 32 * u + lane, p.Sq - 1);
-        pre_l[u] = __ldg(p.lse + base + row);
-        pre_d[u] = __ldg(p.delta + base + row);
+        pre_l[u] = ld_nc_f32(p.lse + base + row);
+        pre_d[u] = ld_nc_f32(p.delta + base + row);
       }
     };
     if (nsteps > 0) fetch(0);
