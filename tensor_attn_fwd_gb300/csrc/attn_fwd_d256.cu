@@ -62,6 +62,10 @@ constexpr size_t kSmem256 = 1024 + size_t(kQBytes) + size_t(kStages256) * kHalfB
 static_assert(kSmem256 <= 232448, "shared memory per CTA");
 constexpr uint32_t kIdescQK256 = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV256 = idesc_bf16_f32(128, 128, false, true);
+// O (all 256 columns) += P V in one MMA per 16 keys, when V's two halves sit
+// in consecutive ring slots: their four 64-column sub-tiles are then evenly
+// spaced (the descriptor's 16 KB leading-byte offset) from the first slot.
+constexpr uint32_t kIdescPVWide = idesc_bf16_f32(128, 256, false, true);
 
 struct Bars256 {
   uint64_t q_full, q_empty;
@@ -320,22 +324,36 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
       const uint32_t buf = g_pv & 1;
       const uint32_t a = tmem + (buf ? kColS1 : kColS0);
       const uint32_t par = (g_pv >> 1) & 1;
+      const bool wide = v1 == v0 + 1;  // no wrap between the halves
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         good &= wait_bar(&bars->p_full[buf][half], par, bars);
         tc_fence_after();
-#pragma unroll
-        for (int vh = 0; vh < 2; ++vh) {
-          const uint32_t b0 = v_lo + (vh ? v1 : v0) * kHalf16;
-          const uint32_t d = tmem + kColO + vh * 128;
+        if (wide) {
+          const uint32_t b0 = v_lo + v0 * kHalf16;
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
             const uint64_t bd = desc_from_words(b0 + kk * (2048 >> 4), kHi);
             if (j == 0 && kk == 0)
-              mma_ts_w<0>(d, a + kk * 8, bd, kIdescPV256);
+              mma_ts_w<0>(tmem + kColO, a + kk * 8, bd, kIdescPVWide);
             else
-              mma_ts_w<1>(d, a + kk * 8, bd, kIdescPV256);
+              mma_ts_w<1>(tmem + kColO, a + kk * 8, bd, kIdescPVWide);
+          }
+        } else {
+#pragma unroll
+          for (int vh = 0; vh < 2; ++vh) {
+            const uint32_t b0 = v_lo + (vh ? v1 : v0) * kHalf16;
+            const uint32_t d = tmem + kColO + vh * 128;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = half * 4 + k4;
+              const uint64_t bd = desc_from_words(b0 + kk * (2048 >> 4), kHi);
+              if (j == 0 && kk == 0)
+                mma_ts_w<0>(d, a + kk * 8, bd, kIdescPV256);
+              else
+                mma_ts_w<1>(d, a + kk * 8, bd, kIdescPV256);
+            }
           }
         }
       }
