@@ -250,6 +250,21 @@ ATTN_API const char *attn_status_string(int status);
  */
 ATTN_API int attn_debug_status(void *stream);
 
+/*
+ * Self-test of the kernels' bounded waits (failure detection without a fault).
+ * Launches one thread that waits on an mbarrier nothing ever arrives on, with
+ * the loop every kernel's waits use, until `limit_ns` nanoseconds have passed;
+ * it then records ATTN_ERR_TIMEOUT in the device status word -- as a kernel
+ * whose producer stalled would -- and returns.  The context stays usable.
+ *   limit_ns   1,000 .. 1,000,000,000 (else ATTN_ERR_INVALID_ARG)
+ *   waited_ns  device pointer (8-byte aligned) that receives the time the wait
+ *              took, or NULL
+ * Returns ATTN_OK once the kernel is enqueued on `stream`; read the outcome
+ * with attn_debug_status().  Not for the hot path.
+ */
+ATTN_API int attn_wait_selftest(unsigned long long limit_ns, unsigned long long *waited_ns,
+                                void *stream);
+
 /* Library ABI version, (major << 16) | minor. */
 ATTN_API int attn_version(void);
 

@@ -35,7 +35,7 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "at
            "attn_rope_table", "attn_qkv_rope", "attn_decode_num_splits",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
-           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]
+           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "attn_wait_selftest"]
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -71,6 +71,7 @@ _SIGNATURES = {
     "attn_bwd": ([_vp] * 10 + [_int] * 7 + [_flt, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
     "attn_debug_status": ([_vp], _int),
+    "attn_wait_selftest": ([ctypes.c_ulonglong, _vp, _vp], _int),
     "attn_version": ([], _int),
 }
 
@@ -118,6 +119,20 @@ def _stream_handle(stream) -> int:
 def attn_debug_status(stream=None) -> int:
     """Synchronise ``stream`` and return (and clear) the device status word."""
     return int(load_library().attn_debug_status(_stream_handle(stream)))
+
+
+def attn_wait_selftest(limit_ns: int, stream=None):
+    """Run the bounded-wait self-test kernel (a wait on an mbarrier that nothing
+    arrives on, given up after ``limit_ns``) and return ``(status, waited_ns)``:
+    the device status it left (ATTN_ERR_TIMEOUT when the bounded wait works) and
+    how long the wait took on the device clock."""
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    st = int(load_library().attn_wait_selftest(int(limit_ns), waited.data_ptr(),
+                                                _stream_handle(stream)))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_wait_selftest")
+    status = attn_debug_status(stream)
+    return status, int(waited.item())
 
 
 def _check(cond: bool, msg: str):

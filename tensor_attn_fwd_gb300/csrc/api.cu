@@ -366,6 +366,18 @@ int attn_combine(const float* o_part, const float* lse_part, float* o, float* ls
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int attn_wait_selftest(unsigned long long limit_ns, unsigned long long* waited_ns, void* stream) {
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull) return ATTN_ERR_INVALID_ARG;
+  if (waited_ns != nullptr && (reinterpret_cast<uintptr_t>(waited_ns) & 7u) != 0)
+    return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const cudaError_t e =
+      launch_wait_selftest(limit_ns, status, reinterpret_cast<uint64_t*>(waited_ns),
+                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_debug_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;

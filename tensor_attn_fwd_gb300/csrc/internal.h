@@ -67,6 +67,8 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const f
                             float* delta, int B, int Hq, int Hkv, int Sq, int Sk, int D,
                             int causal, float scale, cudaStream_t stream, int* status);
 
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* status, uint64_t* waited_ns,
+                                 cudaStream_t stream);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,
                            int rows, int D, int num_splits, cudaStream_t stream);
 

@@ -80,8 +80,8 @@ __device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// after ATTN_WAIT_NS of polling (the caller reports a timeout).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// after limit_ns of polling (the caller reports a timeout).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -89,8 +89,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer() - t0 > ATTN_WAIT_NS) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, ATTN_WAIT_NS);
 }
 
 // ---------------------------------------------------------------- proxies

@@ -236,3 +236,15 @@ def test_decode_rejects_too_many_rows(lib):
     # (every other limit holds: B*Hkv*Sk*D and ns*B*Hq*D are small, Hkv*slices <= 65535)
     assert dec(lib, B=65535, Hq=32768, Hkv=1, Sk=1, D=64, ns=1) == attn.ATTN_ERR_UNSUPPORTED
     assert dec(lib, B=32768, Hq=32768, Hkv=1, Sk=1, D=64, ns=1, q=None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_wait_selftest_rejects(lib):
+    """The bounded-wait self-test checks its limit and its output pointer
+    before launching anything."""
+    ull = ctypes.c_ulonglong
+    lib.attn_wait_selftest.argtypes = [ull, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.attn_wait_selftest(ull(0), None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_wait_selftest(ull(999), None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_wait_selftest(ull(1_000_000_001), None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_wait_selftest(ull(1_000_000), ctypes.c_void_p(4), None) == \
+        attn.ATTN_ERR_MISALIGNED
