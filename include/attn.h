@@ -81,6 +81,40 @@ ATTN_API int attn_fwd_bf16o(const void *q, const void *k, const void *v, void *o
                             float scale, void *stream);
 
 /*
+ * Prefill forward over KV splits, for shapes with too few (batch, head, 256
+ * query rows) work items to fill the GPU -- chunked prefill, a short query
+ * chunk against a long cache (Sq << Sk).  The same computation as attn_fwd,
+ * cut along the keys as split-KV decode cuts it ([FIBER] Evaluation: decode
+ * and its split-KV combine); the partials are merged by attn_combine.
+ *   Split s covers KV tiles [s*t, (s+1)*t) of 128 keys, t = ceil(ceil(Sk/128) /
+ *   num_splits), with the causal mask of attn_fwd (bottom-right).
+ *   o_part    float [num_splits, B, Hq, Sq, D]: split s's output normalised by
+ *             its own row sum; rows the split leaves without keys get 0.
+ *   lse_part  float [num_splits, B, Hq, Sq]: split s's log-sum-exp, -inf for
+ *             rows without keys.
+ *   Merge with attn_combine(o_part, lse_part, o, lse, B * Sq, Hq, D, num_splits):
+ *   that call reads the partials as num_splits x (B*Hq*Sq rows) x D, which is
+ *   their layout, and writes O [B,Hq,Sq,D] and LSE [B,Hq,Sq].
+ *   1 <= num_splits <= ceil(Sk / 128), else ATTN_ERR_INVALID_ARG; D 64 or 128,
+ *   else ATTN_ERR_UNSUPPORTED.  Other arguments and errors as attn_fwd.
+ */
+ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, float *o_part,
+                              float *lse_part, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                              int causal, int num_splits, float scale, void *stream);
+
+/*
+ * A split count for attn_fwd_splitkv on the current device (a measured rule of
+ * this library, not part of the method).  With B * Hq * ceil(Sq / 256) work
+ * items already filling at least 80 % of the SMs, 1 (use attn_fwd); otherwise
+ * the largest count that still runs every item in one round on the SMs
+ * (floor(SMs / items)), with at least four 128-key tiles per split.  Always 1
+ * for D = 256.  Host-only: launches nothing.
+ *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes, ATTN_ERR_CUDA if the
+ *   device cannot be queried.
+ */
+ATTN_API int attn_fwd_num_splits(int B, int Hq, int Sq, int Sk, int D, int *num_splits);
+
+/*
  * Split-KV decode, first stage: per-split partial results for one query row
  * per head.  Source: same page, Methodology and Evaluation (FlashDecoding:
  * decode is GEMV plus softmax, memory bound, no tensor cores).

@@ -35,7 +35,7 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "at
            "attn_rope_table", "attn_qkv_rope", "attn_decode_num_splits",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
-           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "attn_wait_selftest"]
+           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "attn_wait_selftest", "attn_fwd_splitkv", "attn_fwd_num_splits"]
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -65,6 +65,8 @@ _SIGNATURES = {
                                     _int, _flt, _vp], _int),
     "attn_decode_splitkv_paged": ([_vp] * 7 + [_int] * 8 + [_flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
+    "attn_fwd_splitkv": ([_vp] * 5 + [_int] * 8 + [_flt, _vp], _int),
+    "attn_fwd_num_splits": ([_int] * 5 + [ctypes.POINTER(_int)], _int),
     "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
     "attn_decode_num_splits": ([_int, _int, _int, _int, ctypes.POINTER(_int)], _int),
     "attn_qkv_rope": ([_vp] * 7 + [_int] * 8 + [_vp], _int),
@@ -175,10 +177,13 @@ def _raise_if(status: int, what: str):
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              scale: float | None = None, o: torch.Tensor | None = None,
-             lse: torch.Tensor | None = None, stream=None):
+             lse: torch.Tensor | None = None, stream=None, num_splits=1):
     """Attention forward: O = softmax(Q K^T * scale (+ causal mask)) V and its LSE.
 
     q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] (bf16, contiguous, same device).
+    ``num_splits``: 1 (one pass), an int > 1 (split the keys, then combine:
+    attn_fwd_splitkv + attn_combine, for too few query rows to fill the GPU),
+    or "auto" (attn_fwd_num_splits picks).
     Returns (o [B,Hq,Sq,D] fp32, lse [B,Hq,Sq] fp32).
     """
     _check_bf16("q", q, 4)
@@ -192,6 +197,18 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
         scale = 1.0 / math.sqrt(D)
     o = _out(o, (B, Hq, Sq, D), q.device, "o")
     lse = _out(lse, (B, Hq, Sq), q.device, "lse")
+    if num_splits == "auto":
+        num_splits = attn_fwd_num_splits(B, Hq, Sq, Sk, D, device=q.device)
+    if int(num_splits) > 1:
+        o_part, lse_part = attn_fwd_splitkv(q, k, v, int(num_splits), causal, scale,
+                                            stream=stream)
+        lib = load_library()
+        with torch.cuda.device(q.device):
+            st = lib.attn_combine(o_part.data_ptr(), lse_part.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), B * Sq, Hq, D, int(num_splits),
+                                  _stream_handle(stream))
+        _raise_if(st, "attn_combine")
+        return o, lse
     lib = load_library()
     with torch.cuda.device(q.device):
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
@@ -199,6 +216,44 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
                           float(scale), _stream_handle(stream))
     _raise_if(st, "attn_fwd")
     return o, lse
+
+
+def attn_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
+                     causal: bool = False, scale: float | None = None,
+                     o_part: torch.Tensor | None = None, lse_part: torch.Tensor | None = None,
+                     stream=None):
+    """Prefill forward over ``num_splits`` KV splits: the partials
+    (o_part [ns,B,Hq,Sq,D] fp32, lse_part [ns,B,Hq,Sq] fp32) that attn_combine
+    merges (see include/attn.h)."""
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(k.device == q.device and v.device == q.device, "q/k/v must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ns = int(num_splits)
+    o_part = _out(o_part, (ns, B, Hq, Sq, D), q.device, "o_part")
+    lse_part = _out(lse_part, (ns, B, Hq, Sq), q.device, "lse_part")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_part.data_ptr(),
+                                  lse_part.data_ptr(), B, Hq, Hkv, Sq, Sk, D,
+                                  int(bool(causal)), ns, float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_fwd_splitkv")
+    return o_part, lse_part
+
+
+def attn_fwd_num_splits(B: int, Hq: int, Sq: int, Sk: int, D: int, device=None) -> int:
+    """Split count for attn_fwd_splitkv on ``device`` (measured rule, host only)."""
+    lib = load_library()
+    n = _int(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = lib.attn_fwd_num_splits(int(B), int(Hq), int(Sq), int(Sk), int(D), ctypes.byref(n))
+    _raise_if(st, "attn_fwd_num_splits")
+    return int(n.value)
 
 
 def attn_fwd_bf16o(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,

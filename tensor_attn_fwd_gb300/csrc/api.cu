@@ -188,6 +188,57 @@ int attn_fwd_bf16o(const void* q, const void* k, const void* v, void* o, float* 
   return fwd_common(q, k, v, o, 1, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, stream);
 }
 
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o_part,
+                     float* lse_part, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                     int num_splits, float scale, void* stream) {
+  if (!q || !k || !v || !o_part || !lse_part) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Sq > kMaxSeq || Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+  // Every split covers at least one 128-key tile.
+  if (num_splits < 1 || num_splits > (Sk + 127) / 128) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_splits) * B * Hq * Sq * D > kMaxElems ||
+      static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
+    return ATTN_ERR_UNSUPPORTED;
+  // Work items B*Hq*ceil(Sq/256)*num_splits are indexed with int.
+  if (static_cast<long long>(B) * Hq * ((Sq + 255) / 256) * num_splits > (1ll << 30))
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
+      !aligned16(lse_part))
+    return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const cudaError_t e =
+      launch_attn_fwd_splitkv(q, k, v, o_part, lse_part, B, Hq, Hkv, Sq, Sk, D, causal,
+                              num_splits, scale, static_cast<cudaStream_t>(stream), status);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_num_splits(int B, int Hq, int Sq, int Sk, int D, int* num_splits) {
+  if (num_splits == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return ATTN_ERR_CUDA;
+  long long ns = 1;
+  if (D == 64 || D == 128) {
+    // Work items without splitting: (batch, query head, 256 query rows).
+    const long long base = static_cast<long long>(B) * Hq * ((Sq + 255) / 256);
+    if (base * 5 < static_cast<long long>(n_sm) * 4) {
+      // Too few to fill the GPU: as many splits as still fit every item in one
+      // round on the SMs (a second round would cost as much as it saves), each
+      // split keeping at least four 128-key tiles.
+      ns = n_sm / base > 1 ? n_sm / base : 1;
+      const long long cap = (Sk + 127) / 128 / 4 > 1 ? (Sk + 127) / 128 / 4 : 1;
+      if (ns > cap) ns = cap;
+    }
+  }
+  *num_splits = static_cast<int>(ns);
+  return ATTN_OK;
+}
+
 namespace {
 
 int decode_common(const void* q, const void* k, const void* v, const int* seqlens,

@@ -91,21 +91,27 @@ struct Bars {
 static_assert(sizeof(Bars) <= 256, "barrier block too large");
 
 struct FwdParams {
-  void* o;           // fp32, or bf16 when o_bf16
+  void* o;           // fp32, or bf16 when o_bf16; split s writes at o + s * split_stride_o
   int o_bf16;
-  float* lse;
+  float* lse;        // split s writes at lse + s * split_stride_lse
   int* status;
   int B, Hq, Hkv, Sq, Sk;
   int causal;
   float scale_log2;  // scale * log2(e)
   int num_pairs;     // ceil(Sq / 256)
-  int total_items;   // B * Hq * num_pairs
+  int num_splits;    // KV splits (1: plain forward)
+  int split_tiles;   // KV tiles per split
+  size_t split_stride_o, split_stride_lse;
+  int total_items;   // B * Hq * num_pairs * num_splits
 };
 
 struct Item {
   int bh;      // b * Hq + h
   int q_row0;  // first query row of tile 0
-  int n[2];    // KV tiles needed by query tile 0 / 1 (0: nothing to compute)
+  int split;   // KV split
+  int j0;      // first KV tile of the split
+  int n[2];    // end (exclusive) of query tile 0 / 1's KV tiles in the split;
+               // n[t] <= j0: nothing to compute for tile t
 };
 
 // Number of leading keys that query tile t of an item needs, in KV tiles.
@@ -127,14 +133,21 @@ __device__ __forceinline__ int item_index(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
+// Split-major order: every item of split 0 (the longest) first, then split 1, ...;
+// within a split, highest query rows first.
 __device__ __forceinline__ Item get_item(const FwdParams& p, int idx) {
   const int BH = p.B * p.Hq;
+  const int per_split = BH * p.num_pairs;
   Item it;
-  const int pair = p.num_pairs - 1 - idx / BH;
-  it.bh = idx % BH;
+  it.split = idx / per_split;
+  const int r = idx % per_split;
+  const int pair = p.num_pairs - 1 - r / BH;
+  it.bh = r % BH;
   it.q_row0 = pair * kRowsPerItem;
-  it.n[0] = tile_kv_count(p, it.q_row0);
-  it.n[1] = tile_kv_count(p, it.q_row0 + 128);
+  it.j0 = it.split * p.split_tiles;
+  const int j_end = it.j0 + p.split_tiles;
+  it.n[0] = min(tile_kv_count(p, it.q_row0), j_end);
+  it.n[1] = min(tile_kv_count(p, it.q_row0 + 128), j_end);
   return it;
 }
 
@@ -182,8 +195,8 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
     const Item it = get_item(p, idx);
-    const int n = max(it.n[0], it.n[1]);
-    if (n == 0) continue;
+    const int n = max(it.n[0], it.n[1]);  // end of the item's KV tiles
+    if (n <= it.j0) continue;
     const int b = it.bh / p.Hq, h = it.bh % p.Hq;
     const int bkv = b * p.Hkv + h / group;
     if (q_ctr > 0 && !(ok = wait_warp(&bars->q_empty, (q_ctr - 1) & 1, bars))) break;
@@ -219,12 +232,12 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s)
           tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[st],
-                      s * 64, 0, bkv);
+                      s * 64, it.j0 * 128, bkv);
       }
       __syncwarp();
       ok = __all_sync(0xffffffffu, g);
     }
-    for (int j = 0; j < n && ok; ++j) {
+    for (int j = it.j0; j < n && ok; ++j) {
       uint32_t sv, sk = 0;
       const bool pair = j + 1 < n;
       bool good = take_stage(sv);
@@ -326,13 +339,13 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
     const Item it = get_item(p, idx);
-    const int n = max(it.n[0], it.n[1]);
-    if (n == 0) continue;
+    const int n = max(it.n[0], it.n[1]);  // end of the item's KV tiles
+    if (n <= it.j0) continue;
     if (!(ok = wait_warp(&bars->q_full, q_ctr & 1, bars))) break;
     ++q_ctr;
 
     // Q may be overwritten once the item's last S MMA has completed.
-    int s_left = it.n[0] + it.n[1];
+    int s_left = max(it.n[0] - it.j0, 0) + max(it.n[1] - it.j0, 0);
     auto issue_s_counted = [&](int t, uint32_t st) {
       issue_s(t, st);
       tc_commit_w(&bars->s_full[t]);
@@ -343,11 +356,11 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
     tc_fence_after();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      if (it.n[t] > 0) issue_s_counted(t, kst);
+      if (it.n[t] > it.j0) issue_s_counted(t, kst);
     }
     tc_commit_w(&bars->kv_empty[kst]);
 
-    for (int j = 0; j < n && ok; ++j) {
+    for (int j = it.j0; j < n && ok; ++j) {
       // Both operand tiles of this step are acquired before any P wait, so
       // their (usually already satisfied) waits overlap queued MMAs.
       uint32_t vst, nkst = 0;
@@ -366,7 +379,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
         for (int half = 0; half < 2; ++half) {
           good &= wait_or_abort(&bars->p_full[t][half], p_phase[t], bars);
           tc_fence_after();
-          issue_pv_half(t, vst, half, j == 0);
+          issue_pv_half(t, vst, half, j == it.j0);
         }
         p_phase[t] ^= 1;
         if (j == it.n[t] - 1)
@@ -403,15 +416,18 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
     const Item it = get_item(p, idx);
-    const int nt = it.n[t];
+    const int nt = it.n[t];  // end of this tile's KV tiles in the split
     const int row = it.q_row0 + 128 * t + quad * 32 + lane;
     const bool row_valid = row < p.Sq;
-    const size_t o_off = (static_cast<size_t>(it.bh) * p.Sq + row) * D;
+    const size_t o_off = (static_cast<size_t>(it.bh) * p.Sq + row) * D +
+                         static_cast<size_t>(it.split) * p.split_stride_o;
     float* o_row = static_cast<float*>(p.o) + o_off;
     __nv_bfloat16* o_row16 = static_cast<__nv_bfloat16*>(p.o) + o_off;
-    float* lse_ptr = p.lse + static_cast<size_t>(it.bh) * p.Sq + row;
-    if (nt == 0) {
-      // No key visible to any row of this tile (or the tile is past Sq).
+    float* lse_ptr = p.lse + static_cast<size_t>(it.bh) * p.Sq + row +
+                     static_cast<size_t>(it.split) * p.split_stride_lse;
+    if (nt <= it.j0) {
+      // No key of the split visible to any row of this tile (or the tile is
+      // past Sq): O = 0, LSE = -inf (a split a combine weighs with 0).
       if (row_valid) {
         if (p.o_bf16) {
 #pragma unroll 4
@@ -431,7 +447,7 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
     float m = -INFINITY;  // reference maximum (log2 domain)
     float l = 0.f;
 
-    for (int j = 0; j < nt; ++j) {
+    for (int j = it.j0; j < nt; ++j) {
       ok = __all_sync(0xffffffffu, wait_or_abort(&bars->s_full[t], s_phase, bars));
       if (!ok) break;
       s_phase ^= 1;
@@ -471,7 +487,7 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
 
       bool rescale = false;
       float alpha = 1.f;
-      if (j == 0) {
+      if (j == it.j0) {
         m = m_tile;
       } else if (m_tile - m > kRescaleThreshold) {  // false when both are -inf
         alpha = ex2(m - m_tile);
@@ -648,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o, int o_bf16,
                             float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
-                            float scale, cudaStream_t stream, int* status) {
+                            int num_splits, float scale, cudaStream_t stream, int* status) {
   using C = Cfg<D>;
   CUtensorMap tmQ, tmK, tmV;
   if (!encode_bf16_map(&tmQ, q, D, Sq, B * Hq, 128) || !encode_bf16_map(&tmK, k, D, Sk, B * Hkv, 128) ||
@@ -670,7 +686,12 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_pairs = (Sq + kRowsPerItem - 1) / kRowsPerItem;
-  p.total_items = B * Hq * p.num_pairs;
+  const int kv_tiles = (Sk + 127) / 128;
+  p.num_splits = num_splits;
+  p.split_tiles = (kv_tiles + num_splits - 1) / num_splits;
+  p.split_stride_o = static_cast<size_t>(B) * Hq * Sq * D;
+  p.split_stride_lse = static_cast<size_t>(B) * Hq * Sq;
+  p.total_items = B * Hq * p.num_pairs * num_splits;
   const int grid = p.total_items < sm_count() ? p.total_items : sm_count();
   attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
@@ -685,10 +706,21 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
     return launch_attn_fwd_d256(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
                                 stream, status);
   if (D == 128)
-    return launch_fwd_impl<128>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+    return launch_fwd_impl<128>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, 1, scale,
                                 stream, status);
-  return launch_fwd_impl<64>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream,
-                             status);
+  return launch_fwd_impl<64>(q, k, v, o, o_bf16, lse, B, Hq, Hkv, Sq, Sk, causal, 1, scale,
+                             stream, status);
+}
+
+cudaError_t launch_attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o_part,
+                                    float* lse_part, int B, int Hq, int Hkv, int Sq, int Sk,
+                                    int D, int causal, int num_splits, float scale,
+                                    cudaStream_t stream, int* status) {
+  if (D == 128)
+    return launch_fwd_impl<128>(q, k, v, o_part, 0, lse_part, B, Hq, Hkv, Sq, Sk, causal,
+                                num_splits, scale, stream, status);
+  return launch_fwd_impl<64>(q, k, v, o_part, 0, lse_part, B, Hq, Hkv, Sq, Sk, causal,
+                             num_splits, scale, stream, status);
 }
 
 }  // namespace attn

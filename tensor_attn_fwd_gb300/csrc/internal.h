@@ -44,6 +44,14 @@ struct PagedKV {
 
 // Head dimension 256 (one query tile per CTA, double-buffered S); called by
 // launch_attn_fwd.
+// Prefill over KV splits (D 64 or 128): split s covers KV tiles
+// [s*t, (s+1)*t), t = ceil(ceil(Sk/128) / num_splits), and writes its partial O
+// (fp32, normalised by its own row sum) and LSE at o_part / lse_part + s * the
+// size of one full output; rows a split leaves empty get O = 0, LSE = -inf.
+cudaError_t launch_attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o_part,
+                                    float* lse_part, int B, int Hq, int Hkv, int Sq, int Sk,
+                                    int D, int causal, int num_splits, float scale,
+                                    cudaStream_t stream, int* status);
 cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, void* o, int o_bf16,
                                  float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int causal,
                                  float scale, cudaStream_t stream, int* status);

@@ -248,3 +248,27 @@ def test_wait_selftest_rejects(lib):
     assert lib.attn_wait_selftest(ull(1_000_000_001), None, None) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_wait_selftest(ull(1_000_000), ctypes.c_void_p(4), None) == \
         attn.ATTN_ERR_MISALIGNED
+
+
+def test_fwd_splitkv_rejects(lib):
+    """attn_fwd_splitkv validates before launching: split count within
+    [1, ceil(Sk/128)], D 64 or 128, non-null outputs."""
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd_splitkv.argtypes = [vp] * 5 + [i] * 8 + [f, vp]
+    ptr = vp(256)
+
+    def call(ns=2, D=128, o_part=ptr, Sk=1000):
+        return lib.attn_fwd_splitkv(ptr, ptr, ptr, o_part, ptr, 1, 4, 2, 64, Sk, D, 1, ns,
+                                    f(0.1), None)
+    assert call(ns=0) == attn.ATTN_ERR_INVALID_ARG
+    assert call(ns=9, Sk=1000) == attn.ATTN_ERR_INVALID_ARG   # 8 tiles of 128 keys
+    assert call(D=256) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(o_part=None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_fwd_num_splits_rejects(lib):
+    n = ctypes.c_int(0)
+    lib.attn_fwd_num_splits.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
+    assert lib.attn_fwd_num_splits(0, 4, 64, 1000, 128, ctypes.byref(n)) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_num_splits(1, 4, 64, 1000, 128, None) == attn.ATTN_ERR_INVALID_ARG
