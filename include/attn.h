@@ -104,15 +104,17 @@ ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, float
 
 /*
  * A split count for attn_fwd_splitkv on the current device (a measured rule of
- * this library, not part of the method).  With B * Hq * ceil(Sq / 256) work
- * items already filling at least 80 % of the SMs, 1 (use attn_fwd); otherwise
- * the largest count that still runs every item in one round on the SMs
- * (floor(SMs / items)), with at least four 128-key tiles per split.  Always 1
- * for D = 256.  Host-only: launches nothing.
- *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes, ATTN_ERR_CUDA if the
- *   device cannot be queried.
+ * this library, not part of the method).  The prefill's work items are pairs
+ * of 128-row query tiles: B * Hq * ceil(Sq / 256) of them, or B * Hq / 2 when
+ * Sq <= 128 and Hq / Hkv is even (two query heads of one KV group share an
+ * item).  With the items already filling at least 80 % of the SMs, 1 (use
+ * attn_fwd); otherwise the largest count that still runs every item in one
+ * round on the SMs (floor(SMs / items)), with at least four 128-key tiles per
+ * split.  Always 1 for D = 256.  Host-only: launches nothing.
+ *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0,
+ *   ATTN_ERR_CUDA if the device cannot be queried.
  */
-ATTN_API int attn_fwd_num_splits(int B, int Hq, int Sq, int Sk, int D, int *num_splits);
+ATTN_API int attn_fwd_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, int *num_splits);
 
 /*
  * Split-KV decode, first stage: per-split partial results for one query row

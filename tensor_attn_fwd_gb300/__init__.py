@@ -66,7 +66,7 @@ _SIGNATURES = {
     "attn_decode_splitkv_paged": ([_vp] * 7 + [_int] * 8 + [_flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
     "attn_fwd_splitkv": ([_vp] * 5 + [_int] * 8 + [_flt, _vp], _int),
-    "attn_fwd_num_splits": ([_int] * 5 + [ctypes.POINTER(_int)], _int),
+    "attn_fwd_num_splits": ([_int] * 6 + [ctypes.POINTER(_int)], _int),
     "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
     "attn_decode_num_splits": ([_int, _int, _int, _int, ctypes.POINTER(_int)], _int),
     "attn_qkv_rope": ([_vp] * 7 + [_int] * 8 + [_vp], _int),
@@ -198,7 +198,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     o = _out(o, (B, Hq, Sq, D), q.device, "o")
     lse = _out(lse, (B, Hq, Sq), q.device, "lse")
     if num_splits == "auto":
-        num_splits = attn_fwd_num_splits(B, Hq, Sq, Sk, D, device=q.device)
+        num_splits = attn_fwd_num_splits(B, Hq, Hkv, Sq, Sk, D, device=q.device)
     if int(num_splits) > 1:
         o_part, lse_part = attn_fwd_splitkv(q, k, v, int(num_splits), causal, scale,
                                             stream=stream)
@@ -246,12 +246,14 @@ def attn_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_spli
     return o_part, lse_part
 
 
-def attn_fwd_num_splits(B: int, Hq: int, Sq: int, Sk: int, D: int, device=None) -> int:
+def attn_fwd_num_splits(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int,
+                        device=None) -> int:
     """Split count for attn_fwd_splitkv on ``device`` (measured rule, host only)."""
     lib = load_library()
     n = _int(0)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        st = lib.attn_fwd_num_splits(int(B), int(Hq), int(Sq), int(Sk), int(D), ctypes.byref(n))
+        st = lib.attn_fwd_num_splits(int(B), int(Hq), int(Hkv), int(Sq), int(Sk), int(D),
+                                     ctypes.byref(n))
     _raise_if(st, "attn_fwd_num_splits")
     return int(n.value)
 

@@ -217,15 +217,16 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o_part,
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_fwd_num_splits(int B, int Hq, int Sq, int Sk, int D, int* num_splits) {
+int attn_fwd_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, int* num_splits) {
   if (num_splits == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
   const int n_sm = sm_count();
   if (n_sm <= 0) return ATTN_ERR_CUDA;
   long long ns = 1;
   if (D == 64 || D == 128) {
-    // Work items without splitting: (batch, query head, 256 query rows).
-    const long long base = static_cast<long long>(B) * Hq * ((Sq + 255) / 256);
+    // Work items without splitting (two 128-row query tiles each).
+    const long long base = fwd_items_per_split(B, Hq, Hkv, Sq);
     if (base * 5 < static_cast<long long>(n_sm) * 4) {
       // Too few to fill the GPU: as many splits as still fit every item in one
       // round on the SMs (a second round would cost as much as it saves), each

@@ -99,15 +99,20 @@ struct FwdParams {
   int causal;
   float scale_log2;  // scale * log2(e)
   int num_pairs;     // ceil(Sq / 256)
+  int head_pairs;    // 1: an item is rows [0,128) of two query heads of one KV group
   int num_splits;    // KV splits (1: plain forward)
   int split_tiles;   // KV tiles per split
   size_t split_stride_o, split_stride_lse;
-  int total_items;   // B * Hq * num_pairs * num_splits
+  int total_items;   // B * Hq * num_pairs * num_splits (B * Hq / 2 * num_splits in pairs)
 };
 
+// A work item is two 128-row query tiles that stream the same K/V: rows
+// [256i, 256i+128) and [256i+128, 256i+256) of one query head, or, when
+// Sq <= 128 and the KV groups have an even number of heads, rows [0,128) of
+// query heads 2k and 2k+1 (the same KV head), so that both tiles have rows.
 struct Item {
-  int bh;      // b * Hq + h
-  int q_row0;  // first query row of tile 0
+  int bh;      // b * Hq + h of query tile 0; tile 1's is bh + head_pairs
+  int q_row0;  // first query row of tile 0; tile 1's is q_row0 + 128 (0 in head pairs)
   int split;   // KV split
   int j0;      // first KV tile of the split
   int n[2];    // end (exclusive) of query tile 0 / 1's KV tiles in the split;
@@ -133,21 +138,34 @@ __device__ __forceinline__ int item_index(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
+__device__ __forceinline__ int tile_row0(const FwdParams& p, const Item& it, int t) {
+  return it.q_row0 + (p.head_pairs ? 0 : 128 * t);
+}
+__device__ __forceinline__ int tile_bh(const FwdParams& p, const Item& it, int t) {
+  return it.bh + (p.head_pairs ? t : 0);
+}
+
 // Split-major order: every item of split 0 (the longest) first, then split 1, ...;
 // within a split, highest query rows first.
 __device__ __forceinline__ Item get_item(const FwdParams& p, int idx) {
   const int BH = p.B * p.Hq;
-  const int per_split = BH * p.num_pairs;
   Item it;
-  it.split = idx / per_split;
-  const int r = idx % per_split;
-  const int pair = p.num_pairs - 1 - r / BH;
-  it.bh = r % BH;
-  it.q_row0 = pair * kRowsPerItem;
+  if (p.head_pairs) {
+    const int per_split = BH / 2;
+    it.split = idx / per_split;
+    it.bh = 2 * (idx % per_split);
+    it.q_row0 = 0;
+  } else {
+    const int per_split = BH * p.num_pairs;
+    it.split = idx / per_split;
+    const int r = idx % per_split;
+    it.bh = r % BH;
+    it.q_row0 = (p.num_pairs - 1 - r / BH) * kRowsPerItem;
+  }
   it.j0 = it.split * p.split_tiles;
   const int j_end = it.j0 + p.split_tiles;
   it.n[0] = min(tile_kv_count(p, it.q_row0), j_end);
-  it.n[1] = min(tile_kv_count(p, it.q_row0 + 128), j_end);
+  it.n[1] = min(tile_kv_count(p, tile_row0(p, it, 1)), j_end);
   return it;
 }
 
@@ -197,7 +215,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
     const Item it = get_item(p, idx);
     const int n = max(it.n[0], it.n[1]);  // end of the item's KV tiles
     if (n <= it.j0) continue;
-    const int b = it.bh / p.Hq, h = it.bh % p.Hq;
+    const int b = it.bh / p.Hq, h = it.bh % p.Hq;  // both tiles' KV head
     const int bkv = b * p.Hkv + h / group;
     if (q_ctr > 0 && !(ok = wait_warp(&bars->q_empty, (q_ctr - 1) & 1, bars))) break;
     if (elect_one()) {
@@ -207,7 +225,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s)
           tma_load_3d(sQ + t * C::kTileBytes + s * kSubBytes, tmQ, &bars->q_full, s * 64,
-                      it.q_row0 + 128 * t, it.bh);
+                      tile_row0(p, it, t), tile_bh(p, it, t));
     }
     __syncwarp();
     ++q_ctr;
@@ -416,14 +434,17 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
     const Item it = get_item(p, idx);
-    const int nt = it.n[t];  // end of this tile's KV tiles in the split
-    const int row = it.q_row0 + 128 * t + quad * 32 + lane;
+    // This warpgroup's tile (t is a runtime value: select, do not index, so the
+    // item stays in registers).
+    const int nt = t ? it.n[1] : it.n[0];  // end of this tile's KV tiles in the split
+    const int bh = tile_bh(p, it, t);
+    const int row = tile_row0(p, it, t) + quad * 32 + lane;
     const bool row_valid = row < p.Sq;
-    const size_t o_off = (static_cast<size_t>(it.bh) * p.Sq + row) * D +
+    const size_t o_off = (static_cast<size_t>(bh) * p.Sq + row) * D +
                          static_cast<size_t>(it.split) * p.split_stride_o;
     float* o_row = static_cast<float*>(p.o) + o_off;
     __nv_bfloat16* o_row16 = static_cast<__nv_bfloat16*>(p.o) + o_off;
-    float* lse_ptr = p.lse + static_cast<size_t>(it.bh) * p.Sq + row +
+    float* lse_ptr = p.lse + static_cast<size_t>(bh) * p.Sq + row +
                      static_cast<size_t>(it.split) * p.split_stride_lse;
     if (nt <= it.j0) {
       // No key of the split visible to any row of this tile (or the tile is
@@ -686,12 +707,13 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_pairs = (Sq + kRowsPerItem - 1) / kRowsPerItem;
+  p.head_pairs = fwd_head_pairs(Hq, Hkv, Sq);
   const int kv_tiles = (Sk + 127) / 128;
   p.num_splits = num_splits;
   p.split_tiles = (kv_tiles + num_splits - 1) / num_splits;
   p.split_stride_o = static_cast<size_t>(B) * Hq * Sq * D;
   p.split_stride_lse = static_cast<size_t>(B) * Hq * Sq;
-  p.total_items = B * Hq * p.num_pairs * num_splits;
+  p.total_items = static_cast<int>(fwd_items_per_split(B, Hq, Hkv, Sq) * num_splits);
   const int grid = p.total_items < sm_count() ? p.total_items : sm_count();
   attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();

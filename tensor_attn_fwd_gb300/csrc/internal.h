@@ -44,6 +44,16 @@ struct PagedKV {
 
 // Head dimension 256 (one query tile per CTA, double-buffered S); called by
 // launch_attn_fwd.
+// Work items of the D 64/128 prefill per KV split: pairs of 128-row query tiles,
+// either of one head (rows 256i..256i+255) or, when Sq <= 128 and the KV groups
+// have an even number of query heads, of two heads of one group.
+inline int fwd_head_pairs(int Hq, int Hkv, int Sq) {
+  return (Sq <= 128 && (Hq / Hkv) % 2 == 0) ? 1 : 0;
+}
+inline long long fwd_items_per_split(long long B, int Hq, int Hkv, int Sq) {
+  return fwd_head_pairs(Hq, Hkv, Sq) ? B * Hq / 2 : B * Hq * ((Sq + 255) / 256);
+}
+
 // Prefill over KV splits (D 64 or 128): split s covers KV tiles
 // [s*t, (s+1)*t), t = ceil(ceil(Sk/128) / num_splits), and writes its partial O
 // (fp32, normalised by its own row sum) and LSE at o_part / lse_part + s * the

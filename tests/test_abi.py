@@ -268,7 +268,9 @@ def test_fwd_splitkv_rejects(lib):
 
 def test_fwd_num_splits_rejects(lib):
     n = ctypes.c_int(0)
-    lib.attn_fwd_num_splits.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
-    assert lib.attn_fwd_num_splits(0, 4, 64, 1000, 128, ctypes.byref(n)) == \
+    lib.attn_fwd_num_splits.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int)]
+    assert lib.attn_fwd_num_splits(0, 4, 2, 64, 1000, 128, ctypes.byref(n)) == \
         attn.ATTN_ERR_INVALID_ARG
-    assert lib.attn_fwd_num_splits(1, 4, 64, 1000, 128, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_num_splits(1, 4, 3, 64, 1000, 128, ctypes.byref(n)) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_num_splits(1, 4, 2, 64, 1000, 128, None) == attn.ATTN_ERR_INVALID_ARG

@@ -85,14 +85,35 @@ def test_partials_of_keyless_splits():
 
 def test_auto_split_count():
     # Few work items (B * Hq * ceil(Sq/256) = 4) against a long cache: splits.
-    ns = attn.attn_fwd_num_splits(1, 4, 200, 8192, 128)
+    ns = attn.attn_fwd_num_splits(1, 4, 2, 200, 8192, 128)
     assert 1 < ns <= 8192 // 128 // 4
     assert 4 * ns <= torch.cuda.get_device_properties(0).multi_processor_count
     # Enough items to fill the GPU: one pass.
-    assert attn.attn_fwd_num_splits(4, 32, 8192, 8192, 128) == 1
-    assert attn.attn_fwd_num_splits(1, 4, 200, 8192, 256) == 1
+    assert attn.attn_fwd_num_splits(4, 32, 8, 8192, 8192, 128) == 1
+    assert attn.attn_fwd_num_splits(1, 4, 2, 200, 8192, 256) == 1
     q, k, v = make_qkv(1, 4, 2, 200, 3000, 128, seed=11)
     o, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits="auto")
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 128 ** -0.5)
     assert_close(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "auto")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,ns", [
+    (1, 8, 2, 128, 1000, 128, True, 1),    # Sq = 128, groups of 4: heads paired per item
+    (2, 8, 1, 16, 700, 64, False, 1),      # MQA, a few query rows
+    (1, 8, 4, 100, 100, 128, True, 1),     # Sq = Sk
+    (1, 8, 2, 77, 2000, 128, True, 4),     # paired heads over KV splits
+    (1, 6, 2, 100, 300, 128, True, 1),     # groups of 3: no pairing
+])
+def test_short_chunks_match_oracle(B, Hq, Hkv, Sq, Sk, D, causal, ns):
+    """Sq <= 128 with an even number of query heads per KV group: an item holds
+    rows [0,128) of two heads of one group (both tiles have rows)."""
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Sk, D, seed=31 * Sq + Sk + Hq)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale,
+                           num_splits=ns)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    assert_close(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
+                 f"B{B} Hq{Hq} Hkv{Hkv} Sq{Sq} Sk{Sk} ns{ns}")
