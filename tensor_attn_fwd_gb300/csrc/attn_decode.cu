@@ -41,6 +41,7 @@ constexpr int kRows = 16;    // query heads per CTA: the M rows of the MMA
 constexpr int kBlk = 32;     // keys per block
 constexpr int kWarps = 4;    // warps per CTA
 constexpr int kSlots = 3;    // ring slots per warp
+constexpr int kPidBlocks = 32;  // paged: page ids looked up ahead per warp (one per lane)
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLazyRescale = 8.0f;
 
@@ -51,8 +52,10 @@ struct DecCfg {
   static constexpr uint32_t kSlotBytes = kSub * kSubBytes;  // one K or V block
   static constexpr size_t kRingBytes = size_t(kWarps) * kSlots * kSlotBytes;
   static constexpr size_t kStatBytes = 2 * kWarps * kRows * sizeof(float);
+  // Paged caches: the page ids of each warp's first kPidBlocks blocks.
+  static constexpr size_t kPidBytes = size_t(kWarps) * kPidBlocks * sizeof(int);
   static constexpr size_t kSmemBytes =
-      1024 + kRingBytes + kStatBytes + kWarps * kSlots * sizeof(uint64_t);
+      1024 + kRingBytes + kStatBytes + kWarps * kSlots * sizeof(uint64_t) + kPidBytes;
   // The per-warp partial outputs reuse the ring once streaming is over.
   static_assert(size_t(kWarps) * kRows * D * sizeof(float) <= kRingBytes, "ring reuse");
 };
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   float* red_m = reinterpret_cast<float*>(smem + C::kRingBytes);  // [warp][row]
   float* red_l = red_m + kWarps * kRows;                           // [warp][row]
   uint64_t* full = reinterpret_cast<uint64_t*>(red_l + kWarps * kRows);  // [warp][slot]
+  int* pids = reinterpret_cast<int*>(full + kWarps * kSlots);              // [warp][block]
   float* red_o = reinterpret_cast<float*>(ring);                   // [warp][row][D], after streaming
 
   const int split = blockIdx.x;
@@ -135,11 +139,26 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 
   uint64_t* my_full = full + warp * kSlots;
   uint8_t* my_ring = ring + size_t(warp) * kSlots * C::kSlotBytes;
+  int* my_pids = pids + warp * kPidBlocks;
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) mbar_init(&my_full[s], 1);
     fence_mbar_init();
   }
+  // Page id of a block (key0 is a multiple of 32 and page_size of 32: the
+  // block lies inside one page); a bad table entry is reported and page 0 read.
+  auto page_of = [&](int key0) -> int {
+    int pid = __ldg(block_table + static_cast<size_t>(b) * max_pages + key0 / page_size);
+    if (pid < 0 || pid >= num_pages) {
+      record_status(status, ATTN_ERR_INVALID_ARG);
+      pid = 0;
+    }
+    return pid;
+  };
+  // The warp looks up its first kPidBlocks page ids at once (a lane each), so
+  // the issuing lane does not wait on a table load in front of every copy.
+  if (block_table != nullptr && lane < my_nblk)
+    my_pids[lane] = page_of(key_begin + (warp + lane * kWarps) * kBlk);
   __syncwarp();
 
   // Load number li of this warp: even = K block, odd = V block of its (li/2)-th block.
@@ -149,15 +168,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     uint8_t* dst = my_ring + slot * C::kSlotBytes;
     int plane = bkv, row = key0;
     if (block_table != nullptr) {
-      // key0 is a multiple of 32 and page_size of 32: the block is inside one page.
-      const int page = key0 / page_size;
-      int pid = __ldg(block_table + static_cast<size_t>(b) * max_pages + page);
-      if (pid < 0 || pid >= num_pages) {
-        record_status(status, ATTN_ERR_INVALID_ARG);  // bad table entry: read page 0 instead
-        pid = 0;
-      }
+      const int blk = li >> 1;
+      const int pid = blk < kPidBlocks ? my_pids[blk] : page_of(key0);
       plane = pid * Hkv + g;
-      row = key0 - page * page_size;
+      row = key0 - (key0 / page_size) * page_size;
     }
     mbar_arrive_expect_tx(&my_full[slot], C::kSlotBytes);
 #pragma unroll
