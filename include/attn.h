@@ -129,7 +129,7 @@ ATTN_API int attn_fwd_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, 
  *   q [B,Hq,1,D] bf16;  k, v [B,Hkv,Sk,D] bf16 (contiguous KV per sequence)
  *   o_part [num_splits,B,Hq,D] fp32;  lse_part [num_splits,B,Hq] fp32
  *     (caller-owned workspace, fully overwritten)
- *   1 <= num_splits <= Sk; D in {64, 128}; no mask.
+ *   1 <= num_splits <= Sk; D in {64, 128, 256}; no mask.
  */
 ATTN_API int attn_decode_splitkv(const void *q, const void *k, const void *v, float *o_part,
                         float *lse_part, int B, int Hq, int Hkv, int Sk, int D,
@@ -235,13 +235,15 @@ ATTN_API int attn_qkv_rope(const void *x, const void *w, const float *rope_table
  * measured rule for this library's decode kernel, not part of the method.
  * With B * Hkv * ceil((Hq/Hkv) / 16) CTAs per split already filling at least
  * 80 % of the SMs, one split streams K/V fastest; otherwise about one CTA per
- * SM, with at least 1024 keys per split.  Host-only: launches nothing.
+ * SM (ceil(SMs / CTAs per split); at D = 256, where a CTA takes a whole SM,
+ * floor, so that they run in one wave), with at least 1024 keys per split.
+ * Host-only: launches nothing.
  *
  *   *num_splits receives the count (>= 1, <= max(1, Sk / 1024)).
  *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0,
  *   ATTN_ERR_CUDA if the device cannot be queried.
  */
-ATTN_API int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int *num_splits);
+ATTN_API int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int D, int *num_splits);
 
 /*
  * Split-KV decode, second stage: log-sum-exp combine of the partials.
@@ -251,6 +253,7 @@ ATTN_API int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int *num_spl
  *
  *   o_part [num_splits,B,Hq,D], lse_part [num_splits,B,Hq] (fp32, as written
  *   by attn_decode_splitkv);  o [B,Hq,D] fp32;  lse [B,Hq] fp32.
+ *   D in {64, 128, 256}.
  */
 ATTN_API int attn_combine(const float *o_part, const float *lse_part, float *o, float *lse, int B,
                  int Hq, int D, int num_splits, void *stream);

@@ -68,7 +68,7 @@ _SIGNATURES = {
     "attn_fwd_splitkv": ([_vp] * 5 + [_int] * 8 + [_flt, _vp], _int),
     "attn_fwd_num_splits": ([_int] * 6 + [ctypes.POINTER(_int)], _int),
     "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
-    "attn_decode_num_splits": ([_int, _int, _int, _int, ctypes.POINTER(_int)], _int),
+    "attn_decode_num_splits": ([_int, _int, _int, _int, _int, ctypes.POINTER(_int)], _int),
     "attn_qkv_rope": ([_vp] * 7 + [_int] * 8 + [_vp], _int),
     "attn_bwd": ([_vp] * 10 + [_int] * 7 + [_flt, _vp], _int),
     "attn_status_string": ([_int], ctypes.c_char_p),
@@ -474,12 +474,14 @@ def attn_combine(o_part: torch.Tensor, lse_part: torch.Tensor, o: torch.Tensor |
     return o, lse
 
 
-def attn_decode_num_splits(B: int, Hq: int, Hkv: int, Sk: int, device=None) -> int:
+def attn_decode_num_splits(B: int, Hq: int, Hkv: int, Sk: int, D: int = 128,
+                           device=None) -> int:
     """Split count for the decode kernels on ``device`` (measured rule, host only)."""
     lib = load_library()
     n = _int(0)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        st = lib.attn_decode_num_splits(int(B), int(Hq), int(Hkv), int(Sk), ctypes.byref(n))
+        st = lib.attn_decode_num_splits(int(B), int(Hq), int(Hkv), int(Sk), int(D),
+                                        ctypes.byref(n))
     _raise_if(st, "attn_decode_num_splits")
     return int(n.value)
 
@@ -494,7 +496,7 @@ def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int | 
     """
     if num_splits is None:
         num_splits = attn_decode_num_splits(q.shape[0], q.shape[1], k.shape[1], k.shape[2],
-                                            q.device)
+                                            k.shape[3], q.device)
     o_part, lse_part = (None, None) if workspace is None else workspace
     if seqlens is None:
         o_part, lse_part = attn_decode_splitkv(q, k, v, num_splits, scale, o_part, lse_part,

@@ -259,7 +259,7 @@ int decode_common(const void* q, const void* k, const void* v, const int* seqlen
   const int head_slices = (Hq / Hkv + 15) / 16;  // query heads per decode CTA: 16
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535)
     return ATTN_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
       !aligned16(lse_part))
     return ATTN_ERR_MISALIGNED;
@@ -384,9 +384,10 @@ int attn_qkv_rope(const void* x, const void* w, const float* rope_table, const i
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int* num_splits) {
+int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int D, int* num_splits) {
   if (num_splits == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
   const int n_sm = sm_count();
   if (n_sm <= 0) return ATTN_ERR_CUDA;
   // CTAs without splitting: (batch, KV head, 16-head slice of the group).
@@ -394,8 +395,9 @@ int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int* num_splits) {
   long long ns = 1;
   if (base * 5 < static_cast<long long>(n_sm) * 4) {
     // Too few to stream at full bandwidth: about one CTA per SM, each split
-    // keeping at least 1024 keys.
-    ns = (n_sm + base - 1) / base;
+    // keeping at least 1024 keys.  At D = 256 a decode CTA takes a whole SM,
+    // so the CTAs must fit in one wave: floor instead of ceil.
+    ns = D == 256 ? (n_sm / base > 1 ? n_sm / base : 1) : (n_sm + base - 1) / base;
     const long long cap = Sk / 1024 > 1 ? Sk / 1024 : 1;
     if (ns > cap) ns = cap;
   }
@@ -410,7 +412,7 @@ int attn_combine(const float* o_part, const float* lse_part, float* o, float* ls
   if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems ||
       static_cast<long long>(B) * Hq > (1ll << 30))
     return ATTN_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_MISALIGNED;
   const cudaError_t e = launch_combine(o_part, lse_part, o, lse, B * Hq, D, num_splits,

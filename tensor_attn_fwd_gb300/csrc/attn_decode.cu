@@ -458,12 +458,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       for (int k = 0; k < cnt; ++k) {
         const float w = __shfl_sync(0xffffffffu, w_lane, k);
         const float* src = o_part + (static_cast<size_t>(c0 + k) * rows + row) * D + lane * DPL;
-        if constexpr (DPL == 4) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(src));
-          out[0] = fmaf(w, x.x, out[0]);
-          out[1] = fmaf(w, x.y, out[1]);
-          out[2] = fmaf(w, x.z, out[2]);
-          out[3] = fmaf(w, x.w, out[3]);
+        if constexpr (DPL >= 4) {
+#pragma unroll
+          for (int e = 0; e < DPL; e += 4) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(src + e));
+            out[e] = fmaf(w, x.x, out[e]);
+            out[e + 1] = fmaf(w, x.y, out[e + 1]);
+            out[e + 2] = fmaf(w, x.z, out[e + 2]);
+            out[e + 3] = fmaf(w, x.w, out[e + 3]);
+          }
         } else {
           const float2 x = __ldg(reinterpret_cast<const float2*>(src));
           out[0] = fmaf(w, x.x, out[0]);
@@ -479,8 +482,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     L = M + logf(W);
   }
   float* dst = o + static_cast<size_t>(row) * D + lane * DPL;
-  if constexpr (DPL == 4) {
-    *reinterpret_cast<float4*>(dst) = make_float4(out[0], out[1], out[2], out[3]);
+  if constexpr (DPL >= 4) {
+#pragma unroll
+    for (int e = 0; e < DPL; e += 4)
+      *reinterpret_cast<float4*>(dst + e) = make_float4(out[e], out[e + 1], out[e + 2], out[e + 3]);
   } else {
     *reinterpret_cast<float2*>(dst) = make_float2(out[0], out[1]);
   }
@@ -522,6 +527,9 @@ cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, f
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
                                   int num_splits, float scale, cudaStream_t stream, int* status,
                                   const int* seqlens, const PagedKV* paged) {
+  if (D == 256)
+    return launch_decode_impl<256>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
+                                   num_splits, scale, stream, status);
   if (D == 128)
     return launch_decode_impl<128>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
                                    num_splits, scale, stream, status);
@@ -544,7 +552,9 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (D == 128)
+  if (D == 256)
+    e = cudaLaunchKernelEx(&cfg, combine_kernel<256>, o_part, lse_part, o, lse, rows, num_splits);
+  else if (D == 128)
     e = cudaLaunchKernelEx(&cfg, combine_kernel<128>, o_part, lse_part, o, lse, rows, num_splits);
   else
     e = cudaLaunchKernelEx(&cfg, combine_kernel<64>, o_part, lse_part, o, lse, rows, num_splits);
@@ -604,7 +614,7 @@ extern "C" int attn_decode_noalloc(const void* q, const void* k, const void* v, 
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > Sk) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Hkv * Sk * D > (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
   const int head_slices = (Hq / Hkv + 15) / 16;
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535) return ATTN_ERR_UNSUPPORTED;

@@ -208,9 +208,13 @@ def test_rope_table_rejects(lib, args, code):
 
 def test_decode_num_splits_rejects(lib):
     n = ctypes.c_int(0)
-    assert lib.attn_decode_num_splits(1, 4, 1, 64, None) == attn.ATTN_ERR_INVALID_ARG
-    assert lib.attn_decode_num_splits(0, 4, 1, 64, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
-    assert lib.attn_decode_num_splits(1, 6, 4, 64, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_num_splits(1, 4, 1, 64, 128, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_num_splits(0, 4, 1, 64, 128, ctypes.byref(n)) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_num_splits(1, 6, 4, 64, 128, ctypes.byref(n)) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_num_splits(1, 4, 1, 64, 0, ctypes.byref(n)) == \
+        attn.ATTN_ERR_INVALID_ARG
 
 
 def bwdc(lib, B=1, Hq=2, Hkv=1, Sq=64, Sk=64, D=64, causal=0, scale=0.125, q=A):

@@ -48,6 +48,7 @@ def build_paged(k, v, lens, page, spare_pages, seed):
     (5, 4, 4, 300, 64, 32, 3),
     (3, 16, 1, 2048, 128, 256, 5),
     (4, 32, 8, 4096, 64, 128, 16),
+    (3, 8, 2, 1000, 256, 64, 4),   # D = 256
 ])
 def test_decode_paged(B, Hq, Hkv, cap, D, page, ns):
     q, k, v = make_qkv(B, Hq, Hkv, 1, cap, D, seed=B * 11 + cap + page)

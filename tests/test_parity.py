@@ -167,6 +167,9 @@ def test_decode_workload_full():
     (2, 6, 2, 333, 128, 7),     # group of 3 (partial slice)
     (1, 32, 8, 4096, 128, 1),
     (1, 4, 1, 64, 128, 64),     # one key per split
+    (2, 8, 2, 500, 256, 4),     # D = 256
+    (1, 16, 1, 2000, 256, 7),   # D = 256, MQA, group of 16
+    (3, 6, 2, 33, 256, 5),      # D = 256, ragged, empty splits
 ])
 def test_decode_shapes(B, Hq, Hkv, Sk, D, ns):
     q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=B * 1000 + Sk + ns)
@@ -178,10 +181,11 @@ def test_decode_shapes(B, Hq, Hkv, Sk, D, ns):
     assert_close(o, lse, o_ref[:, :, 0], lse_ref[:, :, 0], "combined")
 
 
-def test_combine_alone_against_oracle():
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_combine_alone_against_oracle(D):
     # Feed the same partials (including empty splits) to both combines.
     g = torch.Generator().manual_seed(3)
-    ns, B, Hq, D = 6, 3, 8, 128
+    ns, B, Hq = 6, 3, 8
     op = torch.randn(ns, B, Hq, D, generator=g)
     lp = torch.randn(ns, B, Hq, generator=g) * 4
     lp[1] = -math.inf
@@ -217,6 +221,7 @@ def test_decode_matches_prefill_kernel():
     (6, 8, 2, 700, 128, 4),
     (5, 4, 4, 300, 64, 3),
     (4, 32, 8, 2048, 128, 8),
+    (4, 8, 2, 900, 256, 3),     # D = 256
 ])
 def test_decode_varlen(B, Hq, Hkv, Sk, D, ns):
     q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=B * 7 + Sk)
@@ -267,22 +272,24 @@ def test_bf16_output(B, Hq, Hkv, Sq, Sk, D, causal):
     assert torch.equal(lse, lse32)
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,Sk,want", [
-    (64, 32, 8, 4096, 1),      # 512 CTAs already fill the SMs
-    (4, 32, 8, 8192, None),    # 32 CTAs: several splits
-    (1, 32, 8, 2048, 2),       # capped at Sk / 1024
-    (1, 4, 1, 500, 1),         # too short to split
+@pytest.mark.parametrize("B,Hq,Hkv,Sk,D,want", [
+    (64, 32, 8, 4096, 128, 1),     # 512 CTAs already fill the SMs
+    (4, 32, 8, 8192, 128, None),   # 32 CTAs: several splits
+    (8, 32, 4, 32768, 256, None),  # D = 256: one CTA per SM, so one wave
+    (1, 32, 8, 2048, 128, 2),      # capped at Sk / 1024
+    (1, 4, 1, 500, 128, 1),        # too short to split
 ])
-def test_decode_num_splits_rule(B, Hq, Hkv, Sk, want):
+def test_decode_num_splits_rule(B, Hq, Hkv, Sk, D, want):
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
-    ns = attn.attn_decode_num_splits(B, Hq, Hkv, Sk)
+    ns = attn.attn_decode_num_splits(B, Hq, Hkv, Sk, D)
     base = B * Hkv * (((Hq // Hkv) + 15) // 16)
-    expect = want if want is not None else min((n_sm + base - 1) // base, max(1, Sk // 1024))
+    per_sm = max(1, n_sm // base) if D == 256 else (n_sm + base - 1) // base
+    expect = want if want is not None else min(per_sm, max(1, Sk // 1024))
     assert ns == expect
     # and the default decode path uses it and matches the oracle
-    q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, 128, seed=B + Sk)
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=B + Sk)
     o, lse = attn.decode(q.cuda(), k.cuda(), v.cuda())
     torch.cuda.synchronize()
     assert attn.attn_debug_status() == attn.ATTN_OK
-    o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(128))
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(D))
     assert_close(o.cpu().numpy(), lse.cpu().numpy(), o_ref[:, :, 0], lse_ref[:, :, 0], "auto splits")
