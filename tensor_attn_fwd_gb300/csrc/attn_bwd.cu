@@ -235,21 +235,30 @@ __device__ __forceinline__ void mma_ts_acc(uint32_t tmem, uint32_t acc_col, uint
   }
 }
 
-// Read a 128-column fp32 accumulator row of this thread from TMEM, scale it and
-// store it to global memory (valid rows only).
+// Read columns [c_begin, c_end) of this thread's fp32 accumulator row from
+// TMEM, scale them and store them to global memory (valid rows only).  Rows
+// are D floats apart and lane l holds row l of its warp's 32; lane pairs swap
+// half their segments (pair_transpose8) so that each store writes 64
+// contiguous bytes of one row.  All 32 lanes must call it.
 template <int D>
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, float* dst, float mul, bool valid,
-                                              int c_begin, int c_end) {
+                                              int c_begin, int c_end, int lane) {
+  const int pb = lane & 1;
+  const bool partner_valid = __shfl_xor_sync(0xffffffffu, valid, 1);
+  const bool even_valid = pb ? partner_valid : valid, odd_valid = pb ? valid : partner_valid;
+  float* even_row = dst - pb * D;
+  const bool v8 = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
 #pragma unroll 1
   for (int c = c_begin; c < c_end; c += 32) {
-    uint32_t r[32];
-    tmem_ld32(taddr + c, r);
-    if (valid) {
+    uint32_t w[32];
+    tmem_ld32(taddr + c, w);
 #pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(dst + c + e) =
-            make_float4(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul,
-                        __uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * mul);
+    pair_transpose8(w, lane);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      if (even_valid) st_global_8w(even_row + c + 8 * (2 * m + pb), &w[16 * m], v8);
+      if (odd_valid) st_global_8w(even_row + D + c + 8 * (2 * m + pb), &w[16 * m + 8], v8);
     }
   }
 }
@@ -519,9 +528,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
           tc_fence_after();
           store_acc_row<D>(tmem + lane_addr + C::kColA0, dk_row, p.scale, key_valid,
-                           half * D / 2, (half + 1) * D / 2);
+                           half * D / 2, (half + 1) * D / 2, lane);
           store_acc_row<D>(tmem + lane_addr + C::kColA1, dv_row, 1.f, key_valid,
-                           half * D / 2, (half + 1) * D / 2);
+                           half * D / 2, (half + 1) * D / 2, lane);
         }
       }
     }
@@ -750,7 +759,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
           tc_fence_after();
           store_acc_row<D>(tmem + lane_addr + C::kColA0, dq_row, p.scale, row_valid,
-                           half * D / 2, (half + 1) * D / 2);
+                           half * D / 2, (half + 1) * D / 2, lane);
         }
       }
     }

@@ -81,6 +81,7 @@ static_assert(sizeof(Bars256) <= 256, "barrier block too large");
 struct Params256 {
   void* o;  // fp32, or bf16 when o_bf16
   int o_bf16;
+  int o_v8;  // o is 32-byte aligned: 32-byte stores
   float* lse;
   int* status;
   int B, Hq, Hkv, Sq, Sk, causal;
@@ -523,27 +524,40 @@ __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem
     if (!ok) break;
     tc_fence_after();
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    // Lane pairs swap half their segments so that each store writes 64
+    // contiguous bytes of a row (as in the D = 64/128 kernel's epilogue).
+    const int pb = lane & 1;
+    const bool even_valid = row - pb < p.Sq, odd_valid = row - pb + 1 < p.Sq;
+    if (p.o_bf16) {
 #pragma unroll 1
-    for (int c = 0; c < kD; c += 32) {
-      uint32_t orow[32];
-      tmem_ld32(tO + c, orow);
-      if (row_valid) {
-        if (p.o_bf16) {
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t w[16];
+        {
+          uint32_t orow[32];
+          tmem_ld32(tO + c, orow);
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(orow[e]) * inv_l, __uint_as_float(orow[e + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(orow[e + 2]) * inv_l, __uint_as_float(orow[e + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(orow[e + 4]) * inv_l, __uint_as_float(orow[e + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(orow[e + 6]) * inv_l, __uint_as_float(orow[e + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(o_row16 + c + e) = w;
-          }
-        } else {
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
+                               __uint_as_float(orow[2 * i + 1]) * inv_l);
+        }
+        pair_transpose8(w, lane);
+        if (even_valid) st_global_8w(o_row16 + (0 - pb) * kD + c + 16 * pb, &w[0], p.o_v8);
+        if (odd_valid) st_global_8w(o_row16 + (1 - pb) * kD + c + 16 * pb, &w[8], p.o_v8);
+      }
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t w[32];
+        tmem_ld32(tO + c, w);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(o_row + c + e) =
-                make_float4(__uint_as_float(orow[e]) * inv_l, __uint_as_float(orow[e + 1]) * inv_l,
-                            __uint_as_float(orow[e + 2]) * inv_l, __uint_as_float(orow[e + 3]) * inv_l);
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * inv_l);
+        pair_transpose8(w, lane);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          if (even_valid)
+            st_global_8w(o_row + (0 - pb) * kD + c + 8 * (2 * m + pb), &w[16 * m], p.o_v8);
+          if (odd_valid)
+            st_global_8w(o_row + (1 - pb) * kD + c + 8 * (2 * m + pb), &w[16 * m + 8], p.o_v8);
         }
       }
     }
@@ -634,6 +648,7 @@ cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, vo
   Params256 p;
   p.o = o;
   p.o_bf16 = o_bf16;
+  p.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   p.lse = lse;
   p.status = status;
   p.B = B;

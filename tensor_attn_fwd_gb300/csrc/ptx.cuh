@@ -628,6 +628,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Eight 32-bit words to global memory: one 32-byte store when `v8` (the
+// address must then be 32-byte aligned), else two 16-byte stores.
+__device__ __forceinline__ void st_global_8w(void* ptr, const uint32_t* w, bool v8) {
+  if (v8) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    uint4* q = static_cast<uint4*>(ptr);
+    q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// Row-per-lane data (as tcgen05.ld 32x32b returns it) rearranged between the
+// two lanes of each pair so that one store step writes 64 contiguous bytes of
+// one row instead of 32 bytes of 32 rows.  w holds N/8 segments of 8 words of
+// the lane's own row; on return lane 2h+b holds, in segment 2m+s, segment
+// 2m+b of row 2h+s.  All 32 lanes must call it.
+template <int N>
+__device__ __forceinline__ void pair_transpose8(uint32_t (&w)[N], int lane) {
+  static_assert(N % 16 == 0, "whole segment pairs");
+  const bool odd = lane & 1;
+#pragma unroll
+  for (int m = 0; m < N / 16; ++m)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t lo = w[16 * m + i], hi = w[16 * m + 8 + i];
+      const uint32_t r = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+      w[16 * m + i] = odd ? r : lo;
+      w[16 * m + 8 + i] = odd ? hi : r;
+    }
+}
+
 // Named barrier among `nthreads` threads (multiple of 32) of this CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -73,7 +73,15 @@ def test_d256_large_sampled():
     assert_close(o_s, lse_s, o_ref, lse_ref, "D256 S8192 sampled")
 
 
-def test_d256_rejected_by_decode_and_backward():
-    q, k, v = make_qkv(1, 2, 1, 1, 64, 256, seed=1)
-    with pytest.raises(attn.AttnError):
-        attn.attn_decode_splitkv(q.cuda(), k.cuda(), v.cuda(), 2)
+def test_d256_backward_and_split_prefill_unsupported():
+    """D = 256 has the one-pass forward and split-KV decode (parity in
+    test_parity); the backward and the split-KV prefill report
+    ATTN_ERR_UNSUPPORTED."""
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 1, 64, 300, 256, seed=1))
+    o, lse = attn.attn_fwd(q, k, v)
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_bwd(q, k, v, o, lse, q)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd_splitkv(q, k, v, 2)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
