@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, kGradThreads);
-    mbar_init(&bars->ds_full, kGradThreads);
+    mbar_init(&bars->p_ready, kGradThreads / 32);  // one arrival per gradient warp
+    mbar_init(&bars->ds_full, kGradThreads / 32);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_ready);
+      mbar_arrive_warp(&bars->p_ready);
       // dS^T = P^T (dP^T - Delta), into this warpgroup's half of the dP^T columns.
       ok = __all_sync(0xffffffffu, bwd_wait(&bars->dp_full, s & 1, bars));
       if (!ok) break;
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      mbar_arrive_warp(&bars->ds_full);
     }
     if (ok) {
       float* dk_row = p.out0 + (static_cast<size_t>(bg) * p.Sk + key) * D;
@@ -584,8 +584,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, kGradThreads);
-    mbar_init(&bars->ds_full, kGradThreads);
+    mbar_init(&bars->p_ready, kGradThreads / 32);  // one arrival per gradient warp
+    mbar_init(&bars->ds_full, kGradThreads / 32);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       // S(s) is in registers: its columns may be overwritten by S(s+1).
       tc_fence_before();
-      mbar_arrive(&bars->p_ready);
+      mbar_arrive_warp(&bars->p_ready);
       // Keys 128s + 64*half + e are visible for e < n_vis (causal limit, Sk).
       const int n_vis = row_valid ? min(max(key_hi - (128 * s + 64 * half) + 1, 0), 64) : 0;
       const bool need_mask = __any_sync(0xffffffffu, n_vis < 64);
@@ -746,7 +746,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      mbar_arrive_warp(&bars->ds_full);
     }
     if (ok) {
       float* dq_row = p.out0 + (static_cast<size_t>(bh) * p.Sq + row) * D;

@@ -562,7 +562,7 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
           // Keys [64*(c/2), 64*(c/2)+64) of P (and any O rescale) are in TMEM.
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&bars->p_full[t][c >> 1]);
+          mbar_arrive_warp(&bars->p_full[t][c >> 1]);
         }
       }
       float rsum = 0.f;
@@ -650,8 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t][0], 128);
-      mbar_init(&bars->p_full[t][1], 128);
+      mbar_init(&bars->p_full[t][0], 4);  // one arrival per softmax warp of the tile
+      mbar_init(&bars->p_full[t][1], 4);
       mbar_init(&bars->o_full[t], 1);
     }
     mbar_init(&bars->mma_done, 1);
