@@ -199,8 +199,9 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* 
 // Inside a KV step the TMA and MMA warps wait without a vote (a vote after
 // every wait costs ~5 % of the step): each lane keeps its own outcome, the warp
 // carries on issuing with in-bounds addresses whatever it is, and one vote per
-// step makes the decision to stop uniform.  A lane that is still polling is
-// waited for by the next elect.sync, so the warp reconverges by itself.
+// step (TMA warp) or per work item (MMA warp) makes the decision to stop
+// uniform.  A lane that is still polling is waited for by the next
+// elect.sync, so the warp reconverges by itself.
 
 // ------------------------------------------------------------------ producer
 template <int D>
@@ -379,12 +380,16 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
     }
     tc_commit_w(&bars->kv_empty[kst]);
 
-    for (int j = it.j0; j < n && ok; ++j) {
+    // One vote per item: after a timed-out wait the abort flag makes every
+    // later wait of the item give up after a few polls, and the MMAs keep
+    // in-bounds operands, so the item runs out quickly and the vote ends it.
+    bool good = true;
+    for (int j = it.j0; j < n; ++j) {
       // Both operand tiles of this step are acquired before any P wait, so
       // their (usually already satisfied) waits overlap queued MMAs.
       uint32_t vst, nkst = 0;
       const bool has_next = j + 1 < n;
-      bool good = acquire_kv(vst);
+      good &= acquire_kv(vst);
       if (has_next) {  // landed with V_j: counted on V_j's barrier
         nkst = kv_ctr % C::kStages;
         ++kv_ctr;
@@ -408,8 +413,8 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
       }
       tc_commit_w(&bars->kv_empty[vst]);
       if (has_next) tc_commit_w(&bars->kv_empty[nkst]);
-      ok = __all_sync(0xffffffffu, good);
     }
+    ok = __all_sync(0xffffffffu, good);
     if (!ok) break;
   }
   if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
