@@ -48,8 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (one pass) of
 # `bench.py --profile prefill|decode`; profiles/ holds the summary.  Reset to
 # None whenever the kernel changes until it is captured again.
-PREFILL_TRAFFIC_BYTES = 419804416 + 221177600
-DECODE_TRAFFIC_BYTES = 1074304768 + 10377216
+PREFILL_TRAFFIC_BYTES = 418319104 + 221361408
+DECODE_TRAFFIC_BYTES = 1074342656 + 10092288
 
 
 def load_peaks():
