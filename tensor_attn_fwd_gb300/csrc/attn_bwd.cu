@@ -367,6 +367,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         issue_dp(0);
         ok = __all_sync(0xffffffffu, got);
       }
+      // One vote after the loop: after a timed-out wait the abort flag makes
+      // every later wait give up after a few polls (operands stay in bounds).
+      bool good = true;
       for (int s = 0; s < nsteps && ok; ++s) {
         const int st = s % kStages;
         const uint32_t q_addr = smem_u32(sRing + st * 2 * C::kTile);
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // rows are the K dimension), then at once S^T(s+1): it overwrites P^T(s)
         // only after dV has read it (same-thread tcgen05 order), and the
         // gradient warps need S^T(s) no more; they compute dS^T(s) meanwhile.
-        bool good = bwd_wait(&bars->p_ready, s & 1, bars);
+        good &= bwd_wait(&bars->p_ready, s & 1, bars);
         tc_fence_after();
         mma_ts_acc<D>(tmem, C::kColA1, C::kColS, do_addr, s == 0);
         if (s + 1 < nsteps) good &= issue_s(s + 1);
@@ -386,8 +389,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, q_addr, s == 0);
         tc_commit_w(&bars->empty[st]);
         if (s + 1 < nsteps) issue_dp(s + 1);
-        ok = __all_sync(0xffffffffu, good);
       }
+      ok = ok && __all_sync(0xffffffffu, good);
       if (ok) tc_commit_w(&bars->acc_full);
       if (!ok) bwd_record(p.status);
       tc_commit_w(&bars->mma_done);
@@ -659,8 +662,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         got &= issue_dp(0);
         ok = __all_sync(0xffffffffu, got);
       }
+      bool good = true;  // one vote after the loop, as in the dK/dV kernel
       for (int s = 0; s < nsteps && ok; ++s) {
-        bool good = true;
         // S(s+1) as soon as the gradient warps have read S(s) ...
         if (s + 1 < nsteps) {
           good &= bwd_wait(&bars->p_ready, s & 1, bars);
@@ -674,8 +677,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_commit_w(&bars->empty[s % kKStages]);
         // ... then dP(s+1), which overwrites dS(s) after dQ has read it.
         if (s + 1 < nsteps) good &= issue_dp(s + 1);
-        ok = __all_sync(0xffffffffu, good);
       }
+      ok = ok && __all_sync(0xffffffffu, good);
       if (ok) tc_commit_w(&bars->acc_full);
       if (!ok) bwd_record(p.status);
       tc_commit_w(&bars->mma_done);
