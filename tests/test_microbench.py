@@ -1,0 +1,33 @@
+"""The sm_103a microbenchmarks: they build without a GPU, and on a GB300 they
+report the rates the kernels' design relies on (one 128x128x16 MMA per ~64
+cycles, twice that at N = 256; the prefill MMA warp's step sequence above its
+2048 MMA cycles)."""
+import os
+import subprocess
+
+import pytest
+
+from tensor_attn_fwd_gb300 import microbench
+
+
+def test_microbench_compiles(tmp_path):
+    out = str(tmp_path / "mb")
+    subprocess.run(microbench.nvcc_command(out), check=True)
+    assert os.path.getsize(out) > 0
+
+
+@pytest.mark.gpu
+def test_microbench_rates():
+    recs = microbench.run()
+    assert not any("error" in r for r in recs), recs
+    mma = {r["shape"]: r["cycles_per_mma"] for r in recs if r["bench"] == "mma_cycles"}
+    assert 50 <= mma["SS M128 N128 K16"] <= 90
+    assert 100 <= mma["SS M128 N256 K16"] <= 180
+    assert 50 <= mma["TS M128 N128 K16"] <= 90
+    (wait,) = [r for r in recs if r["bench"] == "wait_latency"]
+    assert 5 <= wait["cycles_per_try_wait"] <= 500
+    (step,) = [r for r in recs if r["bench"] == "step_sequence"]
+    assert 2000 <= step["cycles_per_step"] <= 4000
+    assert step["cycles_per_step_waits_x4"] > step["cycles_per_step"]
+    (ex2,) = [r for r in recs if r["bench"] == "ex2_rate"]
+    assert ex2["results_per_clock_per_sm"] > 0
