@@ -46,7 +46,9 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. an unsupported D) */
     ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,         /* the CUDA runtime reported an error */
-    ATTN_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (device status) */
+    ATTN_ERR_TIMEOUT = 5,      /* a kernel's bounded wait expired (device status) */
+    ATTN_ERR_BOUNDS = 6        /* debug builds (-DATTN_DEBUG_BOUNDS): a kernel skipped a
+                                  store outside its output buffer (device status) */
 } attn_status;
 
 /*

@@ -35,7 +35,7 @@ __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "at
            "attn_rope_table", "attn_qkv_rope", "attn_decode_num_splits",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
-           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "attn_wait_selftest", "attn_fwd_splitkv", "attn_fwd_num_splits"]
+           "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_BOUNDS", "attn_wait_selftest", "attn_fwd_splitkv", "attn_fwd_num_splits"]
 
 ATTN_OK = 0
 ATTN_ERR_INVALID_ARG = 1
@@ -43,6 +43,7 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_BOUNDS = 6
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libattn.so"

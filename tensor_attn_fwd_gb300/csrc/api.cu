@@ -143,6 +143,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer not 16-byte aligned";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA runtime error";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait expired";
+    case ATTN_ERR_BOUNDS: return "ATTN_ERR_BOUNDS: a kernel store fell outside its output (debug build)";
     default: return "unknown attn status";
   }
 }

@@ -94,6 +94,7 @@ struct FwdParams {
   void* o;           // fp32, or bf16 when o_bf16; split s writes at o + s * split_stride_o
   int o_bf16;
   int o_v8;          // o is 32-byte aligned: 32-byte stores
+  size_t o_bytes, lse_bytes;  // output extents (bounds checks of debug builds)
   float* lse;        // split s writes at lse + s * split_stride_lse
   int* status;
   int B, Hq, Hkv, Sq, Sk;
@@ -455,7 +456,10 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
     if (nt <= it.j0) {
       // No key of the split visible to any row of this tile (or the tile is
       // past Sq): O = 0, LSE = -inf (a split a combine weighs with 0).
-      if (row_valid) {
+      if (row_valid &&
+          store_in_bounds(p.o_bf16 ? static_cast<const void*>(o_row16) : o_row,
+                          D * (p.o_bf16 ? 2 : 4), p.o, p.o_bytes, p.status) &&
+          store_in_bounds(lse_ptr, 4, p.lse, p.lse_bytes, p.status)) {
         if (p.o_bf16) {
 #pragma unroll 4
           for (int c = 0; c < D; c += 8)
@@ -605,8 +609,12 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
                                __uint_as_float(orow[2 * i + 1]) * inv_l);
         }
         pair_transpose8(w, lane);
-        if (even_valid) st_global_8w(o_row16 + (0 - pb) * D + c + 16 * pb, &w[0], p.o_v8);
-        if (odd_valid) st_global_8w(o_row16 + (1 - pb) * D + c + 16 * pb, &w[8], p.o_v8);
+        __nv_bfloat16* e16 = o_row16 + (0 - pb) * D + c + 16 * pb;
+        __nv_bfloat16* d16 = o_row16 + (1 - pb) * D + c + 16 * pb;
+        if (even_valid && store_in_bounds(e16, 32, p.o, p.o_bytes, p.status))
+          st_global_8w(e16, &w[0], p.o_v8);
+        if (odd_valid && store_in_bounds(d16, 32, p.o, p.o_bytes, p.status))
+          st_global_8w(d16, &w[8], p.o_v8);
       }
     } else {
 #pragma unroll 1
@@ -618,14 +626,17 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
         pair_transpose8(w, lane);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          if (even_valid)
-            st_global_8w(o_row + (0 - pb) * D + c + 8 * (2 * m + pb), &w[16 * m], p.o_v8);
-          if (odd_valid)
-            st_global_8w(o_row + (1 - pb) * D + c + 8 * (2 * m + pb), &w[16 * m + 8], p.o_v8);
+          float* e32 = o_row + (0 - pb) * D + c + 8 * (2 * m + pb);
+          float* d32 = o_row + (1 - pb) * D + c + 8 * (2 * m + pb);
+          if (even_valid && store_in_bounds(e32, 32, p.o, p.o_bytes, p.status))
+            st_global_8w(e32, &w[16 * m], p.o_v8);
+          if (odd_valid && store_in_bounds(d32, 32, p.o, p.o_bytes, p.status))
+            st_global_8w(d32, &w[16 * m + 8], p.o_v8);
         }
       }
     }
-    if (row_valid) *lse_ptr = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    if (row_valid && store_in_bounds(lse_ptr, 4, p.lse, p.lse_bytes, p.status))
+      *lse_ptr = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
   }
   if (!ok) record_status(p.status, ATTN_ERR_TIMEOUT);
 }
@@ -718,6 +729,8 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o
   p.o = o;
   p.o_bf16 = o_bf16;
   p.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  p.o_bytes = static_cast<size_t>(num_splits) * B * Hq * Sq * D * (o_bf16 ? 2 : 4);
+  p.lse_bytes = static_cast<size_t>(num_splits) * B * Hq * Sq * sizeof(float);
   p.lse = lse;
   p.status = status;
   p.B = B;

@@ -82,6 +82,7 @@ struct Params256 {
   void* o;  // fp32, or bf16 when o_bf16
   int o_bf16;
   int o_v8;  // o is 32-byte aligned: 32-byte stores
+  size_t o_bytes, lse_bytes;  // output extents (bounds checks of debug builds)
   float* lse;
   int* status;
   int B, Hq, Hkv, Sq, Sk, causal;
@@ -394,7 +395,10 @@ __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem
     __nv_bfloat16* o_row16 = static_cast<__nv_bfloat16*>(p.o) + o_off;
     float* lse_ptr = p.lse + static_cast<size_t>(it.bh) * p.Sq + row;
     if (it.n == 0) {
-      if (row_valid) {
+      if (row_valid &&
+          store_in_bounds(p.o_bf16 ? static_cast<const void*>(o_row16) : o_row,
+                          kD * (p.o_bf16 ? 2 : 4), p.o, p.o_bytes, p.status) &&
+          store_in_bounds(lse_ptr, 4, p.lse, p.lse_bytes, p.status)) {
         if (p.o_bf16) {
 #pragma unroll 4
           for (int c = 0; c < kD; c += 8)
@@ -541,8 +545,12 @@ __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem
                                __uint_as_float(orow[2 * i + 1]) * inv_l);
         }
         pair_transpose8(w, lane);
-        if (even_valid) st_global_8w(o_row16 + (0 - pb) * kD + c + 16 * pb, &w[0], p.o_v8);
-        if (odd_valid) st_global_8w(o_row16 + (1 - pb) * kD + c + 16 * pb, &w[8], p.o_v8);
+        __nv_bfloat16* e16 = o_row16 + (0 - pb) * kD + c + 16 * pb;
+        __nv_bfloat16* d16 = o_row16 + (1 - pb) * kD + c + 16 * pb;
+        if (even_valid && store_in_bounds(e16, 32, p.o, p.o_bytes, p.status))
+          st_global_8w(e16, &w[0], p.o_v8);
+        if (odd_valid && store_in_bounds(d16, 32, p.o, p.o_bytes, p.status))
+          st_global_8w(d16, &w[8], p.o_v8);
       }
     } else {
 #pragma unroll 1
@@ -554,17 +562,20 @@ __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem
         pair_transpose8(w, lane);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          if (even_valid)
-            st_global_8w(o_row + (0 - pb) * kD + c + 8 * (2 * m + pb), &w[16 * m], p.o_v8);
-          if (odd_valid)
-            st_global_8w(o_row + (1 - pb) * kD + c + 8 * (2 * m + pb), &w[16 * m + 8], p.o_v8);
+          float* e32 = o_row + (0 - pb) * kD + c + 8 * (2 * m + pb);
+          float* d32 = o_row + (1 - pb) * kD + c + 8 * (2 * m + pb);
+          if (even_valid && store_in_bounds(e32, 32, p.o, p.o_bytes, p.status))
+            st_global_8w(e32, &w[16 * m], p.o_v8);
+          if (odd_valid && store_in_bounds(d32, 32, p.o, p.o_bytes, p.status))
+            st_global_8w(d32, &w[16 * m + 8], p.o_v8);
         }
       }
     }
     // The TMEM loads of O have completed (tcgen05.wait::ld inside tmem_ld32)
     // before the next item's first product may overwrite O: that product
     // waits for P of the next step, which these threads write after this.
-    if (row_valid) *lse_ptr = l > 0.f ? (m + log2f(l)) * kLn2f : -INFINITY;
+    if (row_valid && store_in_bounds(lse_ptr, 4, p.lse, p.lse_bytes, p.status))
+      *lse_ptr = l > 0.f ? (m + log2f(l)) * kLn2f : -INFINITY;
   }
   if (!ok) note_status(p.status, ATTN_ERR_TIMEOUT);
 }
@@ -649,6 +660,8 @@ cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, vo
   p.o = o;
   p.o_bf16 = o_bf16;
   p.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  p.o_bytes = static_cast<size_t>(B) * Hq * Sq * kD * (o_bf16 ? 2 : 4);
+  p.lse_bytes = static_cast<size_t>(B) * Hq * Sq * sizeof(float);
   p.lse = lse;
   p.status = status;
   p.B = B;

@@ -11,6 +11,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "../../include/attn.h"
+
 #ifndef ATTN_WAIT_NS
 #define ATTN_WAIT_NS 2000000000ull  // 2 s: far beyond any legitimate wait
 #endif
@@ -674,6 +676,24 @@ __device__ __forceinline__ void pair_transpose8(uint32_t (&w)[N], int lane) {
 // Named barrier among `nthreads` threads (multiple of 32) of this CTA.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Debug builds (-DATTN_DEBUG_BOUNDS): a store of `bytes` bytes at `ptr` must lie
+// inside the output [base, base + size); otherwise the kernel records
+// ATTN_ERR_BOUNDS in its status word and skips the store.  Release builds
+// compile the check to `true`.
+__device__ __forceinline__ bool store_in_bounds(const void* ptr, uint32_t bytes, const void* base,
+                                                size_t size, int* status) {
+#ifdef ATTN_DEBUG_BOUNDS
+  const char* q = static_cast<const char*>(ptr);
+  const char* b = static_cast<const char*>(base);
+  const bool ok = q >= b && q + bytes <= b + size;
+  if (!ok && status != nullptr) atomicCAS(status, 0, static_cast<int>(ATTN_ERR_BOUNDS));
+  return ok;
+#else
+  (void)ptr; (void)bytes; (void)base; (void)size; (void)status;
+  return true;
+#endif
 }
 
 }  // namespace ptx

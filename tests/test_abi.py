@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         s = attn.attn_status_string(code)
         assert s and isinstance(s, str)
     assert "unknown" in attn.attn_status_string(99)

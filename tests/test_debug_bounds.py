@@ -1,0 +1,53 @@
+"""The debug build (-DATTN_DEBUG_BOUNDS): every prefill output store is checked
+against its buffer, and a store outside it would be skipped and reported as
+ATTN_ERR_BOUNDS.  On ragged shapes, every head dimension, both output types and
+an output that is only 16-byte aligned, the debug library reports ATTN_OK and
+writes exactly what the release library writes."""
+import ctypes
+import math
+
+import pytest
+import torch
+
+import tensor_attn_fwd_gb300 as attn
+from tensor_attn_fwd_gb300 import build as attn_build
+from attn_inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dbg():
+    lib = ctypes.CDLL(attn_build.build(debug=True))
+    for fn in (lib.attn_fwd, lib.attn_fwd_bf16o):
+        fn.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    lib.attn_debug_status.argtypes = [ctypes.c_void_p]
+    lib.attn_debug_status.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,bf16o,offset", [
+    (2, 4, 2, 301, 301, 64, True, False, False),
+    (1, 4, 1, 129, 777, 128, True, True, False),
+    (2, 8, 2, 300, 129, 128, False, False, True),
+    (1, 2, 2, 7, 7, 128, True, False, False),
+    (1, 4, 2, 333, 333, 256, True, False, False),
+    (1, 2, 1, 200, 640, 256, False, True, True),
+])
+def test_debug_build_matches_release(dbg, B, Hq, Hkv, Sq, Sk, D, causal, bf16o, offset):
+    q, k, v = (t.cuda() for t in make_qkv(B, Hq, Hkv, Sq, Sk, D, seed=Sq + 3 * Sk + D))
+    fwd = attn.attn_fwd_bf16o if bf16o else attn.attn_fwd
+    o_ref, lse_ref = fwd(q, k, v, causal=causal)
+    dtype = torch.bfloat16 if bf16o else torch.float32
+    off = (16 // torch.tensor([], dtype=dtype).element_size()) if offset else 0
+    numel = B * Hq * Sq * D
+    buf = torch.full((numel + off,), 3.0, dtype=dtype, device="cuda")
+    o = buf[off:].view(B, Hq, Sq, D)
+    lse = torch.full((B, Hq, Sq), 3.0, device="cuda")
+    fn = dbg.attn_fwd_bf16o if bf16o else dbg.attn_fwd
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+            Sq, Sk, D, int(causal), 1.0 / math.sqrt(D), torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK
+    assert dbg.attn_debug_status(None) == attn.ATTN_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
