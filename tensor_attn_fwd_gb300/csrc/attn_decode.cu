@@ -406,11 +406,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         lse = (M + log2f(L)) * kLn2;
       }
       const size_t row = (static_cast<size_t>(split) * B + b) * Hq + hq;
+      const size_t rows = static_cast<size_t>(num_splits) * B * Hq;  // debug bounds checks
       float* dst = o_part + row * D + part * DPT;
+      if (store_in_bounds(dst, DPT * 4, o_part, rows * D * sizeof(float), status)) {
 #pragma unroll
-      for (int e = 0; e < DPT; e += 4)
-        *reinterpret_cast<float4*>(dst + e) = make_float4(out[e], out[e + 1], out[e + 2], out[e + 3]);
-      if (part == 0) lse_part[row] = lse;
+        for (int e = 0; e < DPT; e += 4)
+          *reinterpret_cast<float4*>(dst + e) = make_float4(out[e], out[e + 1], out[e + 2], out[e + 3]);
+      }
+      if (part == 0 && store_in_bounds(lse_part + row, 4, lse_part, rows * sizeof(float), status))
+        lse_part[row] = lse;
     }
   }
   // The combine kernel may now be scheduled; it waits for this grid to finish.

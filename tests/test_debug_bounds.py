@@ -1,4 +1,4 @@
-"""The debug build (-DATTN_DEBUG_BOUNDS): every prefill output store is checked
+"""The debug build (-DATTN_DEBUG_BOUNDS): every prefill and decode output store is checked
 against its buffer, and a store outside it would be skipped and reported as
 ATTN_ERR_BOUNDS.  On ragged shapes, every head dimension, both output types and
 an output that is only 16-byte aligned, the debug library reports ATTN_OK and
@@ -22,6 +22,8 @@ def dbg():
     for fn in (lib.attn_fwd, lib.attn_fwd_bf16o):
         fn.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_void_p]
         fn.restype = ctypes.c_int
+    lib.attn_decode_splitkv.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_void_p]
+    lib.attn_decode_splitkv.restype = ctypes.c_int
     lib.attn_debug_status.argtypes = [ctypes.c_void_p]
     lib.attn_debug_status.restype = ctypes.c_int
     return lib
@@ -51,3 +53,18 @@ def test_debug_build_matches_release(dbg, B, Hq, Hkv, Sq, Sk, D, causal, bf16o, 
     assert st == attn.ATTN_OK
     assert dbg.attn_debug_status(None) == attn.ATTN_OK
     assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sk,D,ns", [(3, 8, 2, 1000, 128, 5), (2, 32, 8, 777, 64, 3),
+                                              (2, 16, 4, 2048, 256, 4)])
+def test_debug_build_decode_matches_release(dbg, B, Hq, Hkv, Sk, D, ns):
+    q, k, v = (t.cuda() for t in make_qkv(B, Hq, Hkv, 1, Sk, D, seed=Sk + D + ns))
+    op_ref, lp_ref = attn.attn_decode_splitkv(q, k, v, ns)
+    op = torch.full_like(op_ref, 3.0)
+    lp = torch.full_like(lp_ref, 3.0)
+    st = dbg.attn_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), op.data_ptr(),
+                                 lp.data_ptr(), B, Hq, Hkv, Sk, D, ns, 1.0 / math.sqrt(D),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK
+    assert dbg.attn_debug_status(None) == attn.ATTN_OK
+    assert torch.equal(op, op_ref) and torch.equal(lp, lp_ref)
