@@ -242,7 +242,8 @@ __device__ __forceinline__ void mma_ts_acc(uint32_t tmem, uint32_t acc_col, uint
 // contiguous bytes of one row.  All 32 lanes must call it.
 template <int D>
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, float* dst, float mul, bool valid,
-                                              int c_begin, int c_end, int lane) {
+                                              int c_begin, int c_end, int lane, const float* base,
+                                              size_t bytes, int* status) {
   const int pb = lane & 1;
   const bool partner_valid = __shfl_xor_sync(0xffffffffu, valid, 1);
   const bool even_valid = pb ? partner_valid : valid, odd_valid = pb ? valid : partner_valid;
@@ -257,8 +258,10 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float* dst, float 
     pair_transpose8(w, lane);
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-      if (even_valid) st_global_8w(even_row + c + 8 * (2 * m + pb), &w[16 * m], v8);
-      if (odd_valid) st_global_8w(even_row + D + c + 8 * (2 * m + pb), &w[16 * m + 8], v8);
+      float* e = even_row + c + 8 * (2 * m + pb);
+      float* o = even_row + D + c + 8 * (2 * m + pb);
+      if (even_valid && store_in_bounds(e, 32, base, bytes, status)) st_global_8w(e, &w[16 * m], v8);
+      if (odd_valid && store_in_bounds(o, 32, base, bytes, status)) st_global_8w(o, &w[16 * m + 8], v8);
     }
   }
 }
@@ -518,9 +521,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) {
       float* dk_row = p.out0 + (static_cast<size_t>(bg) * p.Sk + key) * D;
       float* dv_row = p.out1 + (static_cast<size_t>(bg) * p.Sk + key) * D;
+      const size_t kv_bytes = static_cast<size_t>(p.B) * p.Hkv * p.Sk * D * sizeof(float);
       if (nsteps == 0) {
         // No query row sees these keys: their gradients are zero.
-        if (key_valid) {
+        if (key_valid && store_in_bounds(dk_row, D * 4, p.out0, kv_bytes, p.status) &&
+            store_in_bounds(dv_row, D * 4, p.out1, kv_bytes, p.status)) {
           for (int c = half * D / 2; c < (half + 1) * D / 2; c += 4) {
             *reinterpret_cast<float4*>(dk_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(dv_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -531,9 +536,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
           tc_fence_after();
           store_acc_row<D>(tmem + lane_addr + C::kColA0, dk_row, p.scale, key_valid,
-                           half * D / 2, (half + 1) * D / 2, lane);
+                           half * D / 2, (half + 1) * D / 2, lane, p.out0, kv_bytes, p.status);
           store_acc_row<D>(tmem + lane_addr + C::kColA1, dv_row, 1.f, key_valid,
-                           half * D / 2, (half + 1) * D / 2, lane);
+                           half * D / 2, (half + 1) * D / 2, lane, p.out1, kv_bytes, p.status);
         }
       }
     }
@@ -753,8 +758,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) {
       float* dq_row = p.out0 + (static_cast<size_t>(bh) * p.Sq + row) * D;
+      const size_t q_bytes = static_cast<size_t>(p.B) * p.Hq * p.Sq * D * sizeof(float);
       if (nsteps == 0) {
-        if (row_valid)
+        if (row_valid && store_in_bounds(dq_row, D * 4, p.out0, q_bytes, p.status))
           for (int c = half * D / 2; c < (half + 1) * D / 2; c += 4)
             *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
@@ -762,7 +768,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
           tc_fence_after();
           store_acc_row<D>(tmem + lane_addr + C::kColA0, dq_row, p.scale, row_valid,
-                           half * D / 2, (half + 1) * D / 2, lane);
+                           half * D / 2, (half + 1) * D / 2, lane, p.out0, q_bytes, p.status);
         }
       }
     }

@@ -1,4 +1,4 @@
-"""The debug build (-DATTN_DEBUG_BOUNDS): every prefill and decode output store is checked
+"""The debug build (-DATTN_DEBUG_BOUNDS): every prefill, decode and backward output store is checked
 against its buffer, and a store outside it would be skipped and reported as
 ATTN_ERR_BOUNDS.  On ragged shapes, every head dimension, both output types and
 an output that is only 16-byte aligned, the debug library reports ATTN_OK and
@@ -24,6 +24,8 @@ def dbg():
         fn.restype = ctypes.c_int
     lib.attn_decode_splitkv.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_void_p]
     lib.attn_decode_splitkv.restype = ctypes.c_int
+    lib.attn_bwd.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_void_p]
+    lib.attn_bwd.restype = ctypes.c_int
     lib.attn_debug_status.argtypes = [ctypes.c_void_p]
     lib.attn_debug_status.restype = ctypes.c_int
     return lib
@@ -68,3 +70,22 @@ def test_debug_build_decode_matches_release(dbg, B, Hq, Hkv, Sk, D, ns):
     assert st == attn.ATTN_OK
     assert dbg.attn_debug_status(None) == attn.ATTN_OK
     assert torch.equal(op, op_ref) and torch.equal(lp, lp_ref)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [(1, 4, 2, 301, 64, True), (2, 4, 1, 200, 128, False)])
+def test_debug_build_backward_matches_release(dbg, B, Hq, Hkv, S, D, causal):
+    q, k, v = (t.cuda() for t in make_qkv(B, Hq, Hkv, S, S, D, seed=S + D))
+    g = torch.Generator().manual_seed(S)
+    do = torch.randn((B, Hq, S, D), generator=g).to(torch.bfloat16).cuda()
+    o, lse = attn.attn_fwd(q, k, v, causal=causal)
+    ref = attn.attn_bwd(q, k, v, o, lse, do, causal=causal)
+    dq, dk, dv = (torch.full_like(t, 3.0) for t in ref)
+    ws = torch.empty((B, Hq, S), device="cuda")
+    st = dbg.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                      B, Hq, Hkv, S, S, D, int(causal), 1.0 / math.sqrt(D),
+                      torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK
+    assert dbg.attn_debug_status(None) == attn.ATTN_OK
+    for got, want in zip((dq, dk, dv), ref):
+        assert torch.equal(got, want)
