@@ -241,19 +241,18 @@ int attn_fwd_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, int* num_
   return ATTN_OK;
 }
 
-namespace {
+}  // extern "C"
 
-int decode_common(const void* q, const void* k, const void* v, const int* seqlens,
-                  float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
-                  int num_splits, float scale, void* stream, const PagedKV* paged = nullptr) {
-  if (!q || !k || !v || !o_part || !lse_part) return ATTN_ERR_INVALID_ARG;
+int attn::decode_check_args(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                            int Sk, int D, int num_splits, float scale, bool paged) {
+  if (!q || !k || !v) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (num_splits < 1 || num_splits > Sk) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  // The kernels split [0, Sk) with int arithmetic.
   if (Sk > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
-  if (paged == nullptr && static_cast<long long>(B) * Hkv * Sk * D > kMaxElems)
-    return ATTN_ERR_UNSUPPORTED;
+  if (!paged && static_cast<long long>(B) * Hkv * Sk * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_splits) * B * Hq * D > kMaxElems) return ATTN_ERR_UNSUPPORTED;
   // Output rows (and tensor-map planes) are indexed with int.
   if (static_cast<long long>(B) * Hq > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
@@ -261,9 +260,22 @@ int decode_common(const void* q, const void* k, const void* v, const int* seqlen
   if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535)
     return ATTN_ERR_UNSUPPORTED;
   if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
-      !aligned16(lse_part))
-    return ATTN_ERR_MISALIGNED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+extern "C" {
+
+namespace {
+
+int decode_common(const void* q, const void* k, const void* v, const int* seqlens,
+                  float* o_part, float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
+                  int num_splits, float scale, void* stream, const PagedKV* paged = nullptr) {
+  if (!o_part || !lse_part) return ATTN_ERR_INVALID_ARG;
+  const int chk = decode_check_args(q, k, v, B, Hq, Hkv, Sk, D, num_splits, scale,
+                                    paged != nullptr);
+  if (chk != ATTN_OK) return chk;
+  if (!aligned16(o_part) || !aligned16(lse_part)) return ATTN_ERR_MISALIGNED;
   int* status = status_word_device_ptr();
   if (status == nullptr) return ATTN_ERR_CUDA;
   const cudaError_t e =

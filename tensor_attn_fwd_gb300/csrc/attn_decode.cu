@@ -613,23 +613,16 @@ extern "C" int attn_decode_noalloc(const void* q, const void* k, const void* v, 
                                    float* lse, int B, int Hq, int Hkv, int Sk, int D,
                                    int num_splits, float scale, void* stream) {
   using namespace attn;
-  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sk <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > Sk) return ATTN_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * Hkv * Sk * D > (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
-  const int head_slices = (Hq / Hkv + 15) / 16;
-  if (B > 65535 || static_cast<long long>(Hkv) * head_slices > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!o || !lse) return ATTN_ERR_INVALID_ARG;
+  // The same checks as attn_decode_splitkv (including the sequence-length cap).
+  const int chk = decode_check_args(q, k, v, B, Hq, Hkv, Sk, D, num_splits, scale, false);
+  if (chk != ATTN_OK) return chk;
   // The partials must fit the static scratch array.
   const long long part_floats = static_cast<long long>(num_splits) * B * Hq * D;
   const long long lse_floats = static_cast<long long>(num_splits) * B * Hq;
   if (part_floats + lse_floats > static_cast<long long>(ATTN_NOALLOC_SCRATCH_FLOATS))
     return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16_ptr(q) || !aligned16_ptr(k) || !aligned16_ptr(v) || !aligned16_ptr(o) ||
-      !aligned16_ptr(lse))
-    return ATTN_ERR_MISALIGNED;
+  if (!aligned16_ptr(o) || !aligned16_ptr(lse)) return ATTN_ERR_MISALIGNED;
   float* scratch = decode_scratch_ptr();
   int* status = status_word_device_ptr();
   if (scratch == nullptr || status == nullptr) return ATTN_ERR_CUDA;

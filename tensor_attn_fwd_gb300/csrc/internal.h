@@ -72,6 +72,12 @@ cudaError_t launch_qkv_rope(const void* x, const void* w, const float* rope, con
                             void* q, void* k, void* v, int B, int S, int hidden, int Hq, int Hkv,
                             int D, int max_pos, int style, cudaStream_t stream, int* status);
 
+// The argument checks every split-KV decode entry point shares (inputs, sizes,
+// split count, scale, head dimension, input alignment); `paged` skips the
+// contiguous-cache size limit.  ATTN_OK or the status to return.
+int decode_check_args(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                      int Sk, int D, int num_splits, float scale, bool paged);
+
 // seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).
 // paged: optional page layout (then Sk = max_pages * page_size, the capacity).
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,

@@ -103,6 +103,45 @@ def test_decode_paged_rejects(lib, kw, code):
     assert decp(lib, **kw) == code
 
 
+def noalloc(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=4, Hkv=1, Sk=64, D=128, ns=4, scale=0.1):
+    f = lib.attn_decode_noalloc
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    return f(q, k, v, o, lse, B, Hq, Hkv, Sk, D, ns, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=65), attn.ATTN_ERR_INVALID_ARG),     # more splits than keys
+    (dict(Hq=6, Hkv=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=70000), attn.ATTN_ERR_UNSUPPORTED),
+    # Sequences past 2^30 keys would overflow the kernels' int split arithmetic;
+    # the allocating decode rejects them and so must this one.
+    (dict(Sk=(1 << 30) + 1, ns=8), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Sk=2147483647, ns=8), attn.ATTN_ERR_UNSUPPORTED),
+    # partials beyond the 4 Mi-float scratch array: 8 * 4096 * (128 + 1) floats
+    (dict(B=1024, Hq=4, ns=8), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(k=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(o=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(lse=M), attn.ATTN_ERR_MISALIGNED),
+])
+def test_decode_noalloc_rejects(lib, kw, code):
+    assert noalloc(lib, **kw) == code
+
+
+def test_decode_noalloc_matches_decode_checks(lib):
+    # Every input the allocating decode rejects, the allocation-free one rejects
+    # with the same status (partials pointers aside).
+    for kw in (dict(Sk=(1 << 30) + 1, ns=8), dict(D=96), dict(Hq=6, Hkv=4), dict(ns=0),
+               dict(q=M), dict(scale=0.0)):
+        assert noalloc(lib, **kw) == dec(lib, **kw)
+
+
 def comb(lib, op=A, lp=A, o=A, lse=A, B=1, Hq=4, D=128, ns=4):
     return lib.attn_combine(op, lp, o, lse, B, Hq, D, ns, None)
 

@@ -21,7 +21,8 @@ def run_bench(*args):
 
 @pytest.mark.gpu
 def test_bench_line_has_the_contract_keys():
-    d = run_bench("--steps", "3", "--warmup", "3", "--no-backward", "--no-qkv-rope")
+    d = run_bench("--steps", "3", "--warmup", "3", "--no-backward", "--no-qkv-rope",
+                  "--parity", "sample")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
@@ -41,3 +42,14 @@ def test_bench_line_has_the_contract_keys():
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     dec = d["decode"]
     assert dec["roofline"]["bound"] == "hbm" and dec["value"] > 0
+    # one entry per workload, each tied to an oracle check of its own timed output
+    assert sorted(d["configs"]) == ["C1", "C2", "C3", "C4", "C5"]
+    for name, c in d["configs"].items():
+        assert c["gpu_us"] > 0 and c["value"] > 0, name
+        p = c["parity"]
+        assert p["pass"] is True and p["rows"] >= 1, (name, p)
+        assert p["o_max_abs_err"] <= 2e-2 and p["lse_max_err"] <= 1e-3, (name, p)
+    for name in ("C1", "C2", "C5"):
+        assert d["configs"][name]["parity"]["rows"] == d["configs"][name]["parity"]["rows_total"]
+    assert d["parity_ok"] is True
+    assert d["cpu_baseline"]["cpu_model"]

@@ -5,6 +5,7 @@ Tolerances (bf16 inputs, fp32 accumulation, P rounded to bf16 before P*V):
   LSE: |LSE_gpu - LSE_ref| <= 1e-3 * max(1, |LSE_ref|)
 Rows with no visible key must match exactly (O = 0, LSE = -inf).
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -136,6 +137,20 @@ def test_workload_full_size_sampled_rows(cfg):
     # Every output row is finite and normalised (|O| <= max |V|).
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     assert float(o.abs().max()) <= float(v.float().abs().max()) + 1e-3
+
+
+@pytest.mark.parametrize("cfg,std", [(3, None), (4, None), (4, 2.0)])
+def test_workload_full_size_every_row(cfg, std):
+    # Every element of O and LSE at the full workload sizes against the oracle.
+    # Workload 4's "N(0,2)" is read as variance 2 (std sqrt 2); std = 2 is the
+    # other reading, whose scores are peakier still.
+    w = WORKLOADS[cfg]
+    if std is not None:
+        w = dataclasses.replace(w, name=f"{w.name}_std{std:g}", q_std=std, k_std=std)
+    q, k, v = workload_inputs(w)
+    o, lse = gpu_fwd(q, k, v, w.causal, w.scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.causal, w.scale)
+    assert_close(o, lse, o_ref, lse_ref, w.name)
 
 
 # ---------------------------------------------------------------- decode
