@@ -212,6 +212,11 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
   const int group = p.Hq / p.Hkv;
   uint32_t kv_ctr = 0, q_ctr = 0;
   bool ok = true;
+  // L2 priorities: every query tile is read by one item, every K/V tile by
+  // all items of its KV head (Hq/Hkv heads x the head's query tiles), so K/V
+  // are kept and Q (and, in the softmax role, O) are let go first.
+  const uint64_t pol_q = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_last();
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
@@ -227,8 +232,8 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sQ + t * C::kTileBytes + s * kSubBytes, tmQ, &bars->q_full, s * 64,
-                      tile_row0(p, it, t), tile_bh(p, it, t));
+          tma_load_3d_hint(sQ + t * C::kTileBytes + s * kSubBytes, tmQ, &bars->q_full, s * 64,
+                           tile_row0(p, it, t), tile_bh(p, it, t), pol_q);
     }
     __syncwarp();
     ++q_ctr;
@@ -252,8 +257,8 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
         mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sKV + st * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[st],
-                      s * 64, it.j0 * 128, bkv);
+          tma_load_3d_hint(sKV + st * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[st],
+                           s * 64, it.j0 * 128, bkv, pol_kv);
       }
       __syncwarp();
       ok = __all_sync(0xffffffffu, g);
@@ -267,13 +272,13 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
         mbar_arrive_expect_tx(&bars->kv_full[sv], pair ? 2 * C::kTileBytes : C::kTileBytes);
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sKV + sv * C::kTileBytes + s * kSubBytes, tmV, &bars->kv_full[sv],
-                      s * 64, j * 128, bkv);
+          tma_load_3d_hint(sKV + sv * C::kTileBytes + s * kSubBytes, tmV, &bars->kv_full[sv],
+                           s * 64, j * 128, bkv, pol_kv);
         if (pair) {
 #pragma unroll
           for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sKV + sk * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[sv],
-                        s * 64, (j + 1) * 128, bkv);
+            tma_load_3d_hint(sKV + sk * C::kTileBytes + s * kSubBytes, tmK, &bars->kv_full[sv],
+                             s * 64, (j + 1) * 128, bkv, pol_kv);
           mbar_arrive(&bars->kv_full[sk]);
         }
       }
@@ -434,6 +439,7 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
   const uint32_t tS = tmem + lane_addr + (t ? C::kColS1 : C::kColS0);
   const uint32_t tO = tmem + lane_addr + (t ? C::kColO1 : C::kColO0);
   const float sl2 = p.scale_log2;
+  const uint64_t pol_o = policy_evict_first();  // output rows are written once
   uint32_t s_phase = 0, o_phase = 0;
   bool ok = true;
 
@@ -612,9 +618,9 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
         __nv_bfloat16* e16 = o_row16 + (0 - pb) * D + c + 16 * pb;
         __nv_bfloat16* d16 = o_row16 + (1 - pb) * D + c + 16 * pb;
         if (even_valid && store_in_bounds(e16, 32, p.o, p.o_bytes, p.status))
-          st_global_8w(e16, &w[0], p.o_v8);
+          st_global_8w_hint(e16, &w[0], p.o_v8, pol_o);
         if (odd_valid && store_in_bounds(d16, 32, p.o, p.o_bytes, p.status))
-          st_global_8w(d16, &w[8], p.o_v8);
+          st_global_8w_hint(d16, &w[8], p.o_v8, pol_o);
       }
     } else {
 #pragma unroll 1
@@ -629,9 +635,9 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
           float* e32 = o_row + (0 - pb) * D + c + 8 * (2 * m + pb);
           float* d32 = o_row + (1 - pb) * D + c + 8 * (2 * m + pb);
           if (even_valid && store_in_bounds(e32, 32, p.o, p.o_bytes, p.status))
-            st_global_8w(e32, &w[16 * m], p.o_v8);
+            st_global_8w_hint(e32, &w[16 * m], p.o_v8, pol_o);
           if (odd_valid && store_in_bounds(d32, 32, p.o, p.o_bytes, p.status))
-            st_global_8w(d32, &w[16 * m + 8], p.o_v8);
+            st_global_8w_hint(d32, &w[16 * m + 8], p.o_v8, pol_o);
         }
       }
     }

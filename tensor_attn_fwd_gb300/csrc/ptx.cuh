@@ -130,13 +130,35 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0)
-// with an L2 evict-first hint: streamed data is read exactly once.
+// L2 eviction-priority policies for the cache_hint forms below: evict_first
+// for data touched once (streamed K/V of a decode, Q tiles, output rows),
+// evict_last for tiles many CTAs read again (a KV head's K/V in prefill).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_3d with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int32_t x, int32_t y, int32_t z,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
+      "l"(policy)
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0)
+// under an L2 cache policy.
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar, uint64_t policy) {
@@ -650,6 +672,25 @@ __device__ __forceinline__ void st_global_8w(void* ptr, const uint32_t* w, bool 
     uint4* q = static_cast<uint4*>(ptr);
     q[0] = make_uint4(w[0], w[1], w[2], w[3]);
     q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// st_global_8w under an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void st_global_8w_hint(void* ptr, const uint32_t* w, bool v8,
+                                                  uint64_t policy) {
+  if (v8) {
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                 ::"l"(ptr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                 "r"(w[6]), "r"(w[7]), "l"(policy)
+                 : "memory");
+  } else {
+    char* c = static_cast<char*>(ptr);
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(c),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "l"(policy)
+                 : "memory");
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(c + 16),
+                 "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "l"(policy)
+                 : "memory");
   }
 }
 

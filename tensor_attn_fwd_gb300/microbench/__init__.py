@@ -10,6 +10,11 @@ runs it on the current GPU and returns its measurements as dicts:
   sequence (32 MMAs, 5 waits, 4 commits) with every barrier complete, with each
   wait repeated four times, and the cost of one extra wait between MMA issues.
 - ``ex2_rate``: ex2.approx.f32 results per clock per SM.
+- ``tmem_bw``: bytes per clock per SM moved by tcgen05.ld / tcgen05.st
+  (32x32b shapes) with 4 and with 8 warps per CTA.
+- ``tma_ring_bw``: GB/s of a TMA producer feeding a 6-stage ring of 32 KB
+  stages (two 128 x 64 bf16 boxes, 128B swizzle) whose consumer only releases
+  them: streamed from HBM (1 GiB) and re-read from L2 (38 MiB).
 
 ``python -m tensor_attn_fwd_gb300.microbench`` prints them as JSON lines.
 """

@@ -7,7 +7,17 @@
 //                   (32 MMAs, 5 waits, 4 commits) with every barrier complete,
 //                   and the same with each wait repeated four times
 //   ex2_rate        ex2.approx.f32 results per clock per SM (MUFU)
+//   tmem_bw         bytes per clock per SM that tcgen05.ld / tcgen05.st move
+//                   between TMEM and registers (32x32b shapes, as the softmax
+//                   and epilogue use them), with 4 and 8 warps per CTA
+//   tma_ring_bw     a TMA producer feeding a ring of 32 KB stages (two 128 x 64
+//                   bf16 boxes, 128B swizzle, the prefill K/V tile) and a
+//                   consumer that only releases them: GB/s over all SMs, from
+//                   HBM (1 GiB streamed) and from L2 (a 38 MiB set re-read)
 // Every wait is bounded; every TMEM and shared-memory address is in bounds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cstdio>
 #include <vector>
@@ -207,6 +217,139 @@ __global__ void __launch_bounds__(1024, 1) ex2_rate(long long* out, float* sink,
   if (threadIdx.x == 0) out[blockIdx.x] = t1 - t0;
 }
 
+// TMEM bandwidth.  Warp w reads (or writes) the columns [c0, c0 + 256) of its
+// lane quarter (w % 4) in 64-column loads (two 32x32b.x32 under one wait) or
+// 32-column stores; with 8 warps, warps w and w + 4 take the two column
+// halves.  clock64 around the loop of the slowest warp.
+template <bool STORE>
+__global__ void __launch_bounds__(256, 1) tmem_bw(long long* out, int sweeps, int* status) {
+  __shared__ uint32_t tbase;
+  __shared__ __align__(8) uint64_t fin;
+  if (threadIdx.x < 32) {
+    tmem_alloc(&tbase, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&fin, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const uint32_t cols = nwarps > 4 ? 256u : 512u;
+  const uint32_t c0 = (nwarps > 4 && warp >= 4) ? 256u : 0u;
+  const uint32_t base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0;
+  uint32_t acc = 0;
+  uint32_t r[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) r[i] = threadIdx.x * 64 + i;
+  __syncthreads();
+  const long long t0 = clock64();
+#pragma unroll 1
+  for (int sw = 0; sw < sweeps; ++sw) {
+    if (STORE) {
+#pragma unroll 1
+      for (uint32_t c = 0; c < cols; c += 64) {
+        tmem_st32(base + c, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_st32(base + c + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      }
+      tmem_st_wait();
+    } else {
+#pragma unroll 1
+      for (uint32_t c = 0; c < cols; c += 64) {
+        tmem_ld64(base + c, r);
+#pragma unroll
+        for (int i = 0; i < 64; i += 8) acc ^= r[i];
+      }
+    }
+  }
+  const long long t1 = clock64();
+  __syncthreads();
+  if (acc == 0x9e3779b9u) out[255] = acc;  // keeps the loads
+  if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned long long*>(&out[blockIdx.x]),
+                                         static_cast<unsigned long long>(t1 - t0));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x < 32) tmem_dealloc(tbase, 512);
+  (void)status;
+  (void)fin;
+}
+
+// TMA ring.  CTA b streams `tiles` 128-row tiles of plane b (rows wrap around
+// `rows`) into kRing stages; warp 0 produces, warp 1 waits for each stage and
+// releases it.  Each stage is two [128 x 64] bf16 boxes (32 KB).
+constexpr int kRing = 6;
+constexpr uint32_t kStageBytes = 32768;
+
+__global__ void __launch_bounds__(64, 1) tma_ring(const __grid_constant__ CUtensorMap map,
+                                                  long long* out, int tiles, int rows,
+                                                  int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kRing], empty[kRing];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&map);
+  }
+  __syncthreads();
+  const int tiles_per_plane = rows / 128;
+  bool ok = true;
+  const long long t0 = clock64();
+  if (threadIdx.x < 32) {
+    for (int i = 0; i < tiles && ok; ++i) {
+      const int st = i % kRing;
+      if (i >= kRing) ok = mbar_wait(&empty[st], ((i / kRing) - 1) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok && elect_one()) {
+        mbar_arrive_expect_tx(&full[st], kStageBytes);
+        const int row = (i % tiles_per_plane) * 128;
+        tma_load_3d(sm + st * kStageBytes, &map, &full[st], 0, row, blockIdx.x);
+        tma_load_3d(sm + st * kStageBytes + 16384, &map, &full[st], 64, row, blockIdx.x);
+      }
+      __syncwarp();
+    }
+    // every issued copy lands before the CTA can exit
+    for (int i = (tiles > kRing ? tiles - kRing : 0); i < tiles; ++i)
+      if (!mbar_wait(&full[i % kRing], (i / kRing) & 1)) ok = false;
+  } else {
+    for (int i = 0; i < tiles && ok; ++i) {
+      const int st = i % kRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / kRing) & 1));
+      if (ok && elect_one()) mbar_arrive(&empty[st]);
+      __syncwarp();
+    }
+  }
+  const long long t1 = clock64();
+  if (!ok) atomicExch(status, 1);
+  if (threadIdx.x == 32) out[blockIdx.x] = t1 - t0;
+}
+
+bool encode_ring_map(CUtensorMap* map, void* base, int rows, int planes) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return false;
+  const cuuint64_t dims[3] = {128, cuuint64_t(rows), cuuint64_t(planes)};
+  const cuuint64_t strides[2] = {256, 256 * cuuint64_t(rows)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn)(
+             map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 double median(std::vector<long long> v) {
   std::sort(v.begin(), v.end());
   return static_cast<double>(v[v.size() / 2]);
@@ -281,6 +424,77 @@ int main() {
     if (ok)
       printf("{\"bench\": \"ex2_rate\", \"results_per_clock_per_sm\": %.1f}\n",
              1024.0 * 8.0 * it / median(h));
+  }
+
+  // TMEM bandwidth: 4 and 8 warps, loads and stores.
+  for (int nw = 4; nw <= 8 && ok; nw += 4) {
+    for (int store = 0; store < 2 && ok; ++store) {
+      const int sweeps = 2000;
+      // kSmem of dynamic shared memory keeps one CTA (and one TMEM allocation) per SM
+      cudaFuncSetAttribute(tmem_bw<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      cudaFuncSetAttribute(tmem_bw<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      for (int rep = 0; rep < 2 && ok; ++rep) {
+        cudaMemset(d_out, 0, 256 * sizeof(long long));
+        if (store)
+          tmem_bw<true><<<kGrid, nw * 32, kSmem>>>(d_out, sweeps, d_st);
+        else
+          tmem_bw<false><<<kGrid, nw * 32, kSmem>>>(d_out, sweeps, d_st);
+        ok = cudaDeviceSynchronize() == cudaSuccess;
+      }
+      h.assign(kGrid, 0);
+      cudaMemcpy(h.data(), d_out, kGrid * sizeof(long long), cudaMemcpyDeviceToHost);
+      // 128 lanes x 512 columns x 4 bytes per sweep
+      if (ok)
+        printf("{\"bench\": \"tmem_bw\", \"op\": \"%s\", \"warps\": %d, "
+               "\"bytes_per_clock_per_sm\": %.1f}\n",
+               store ? "st 32x32b.x32" : "ld 32x32b.x32 (x2 per wait)", nw,
+               128.0 * 512 * 4 * sweeps / median(h));
+    }
+  }
+
+  // TMA ring: 1 GiB streamed from HBM once, then a 38 MiB set re-read from L2.
+  if (ok) {
+    const int rows_hbm = 27520;  // 152 planes x 27520 rows x 256 B = 1.07 GB
+    void* buf = nullptr;
+    ok = cudaMalloc(&buf, size_t(kGrid) * rows_hbm * 256) == cudaSuccess;
+    if (ok) cudaMemset(buf, 0, size_t(kGrid) * rows_hbm * 256);
+    const int smem = kRing * kStageBytes + 1024;
+    cudaFuncSetAttribute(tma_ring, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const struct { const char* src; int rows; int tiles; } cases[2] = {
+        {"hbm", rows_hbm, rows_hbm / 128}, {"l2", 1024, 8 * 32}};
+    for (int c = 0; c < 2 && ok; ++c) {
+      CUtensorMap map;
+      ok = encode_ring_map(&map, buf, cases[c].rows, kGrid);
+      if (!ok) break;
+      cudaEvent_t a, b;
+      cudaEventCreate(&a);
+      cudaEventCreate(&b);
+      float best = 1e30f;
+      for (int rep = 0; rep < 3 && ok; ++rep) {
+        if (c == 0) cudaMemset(buf, rep, size_t(kGrid) * rows_hbm * 256);  // evicts L2
+        cudaEventRecord(a);
+        tma_ring<<<kGrid, 64, smem>>>(map, d_out, cases[c].tiles, cases[c].rows, d_st);
+        cudaEventRecord(b);
+        ok = cudaEventSynchronize(b) == cudaSuccess;
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, a, b);
+        best = std::min(best, ms);
+      }
+      h.assign(kGrid, 0);
+      cudaMemcpy(h.data(), d_out, kGrid * sizeof(long long), cudaMemcpyDeviceToHost);
+      int st = 0;
+      cudaMemcpy(&st, d_st, sizeof(int), cudaMemcpyDeviceToHost);
+      ok = ok && st == 0;
+      const double bytes = double(kGrid) * cases[c].tiles * kStageBytes;
+      if (ok)
+        printf("{\"bench\": \"tma_ring_bw\", \"source\": \"%s\", \"stages\": %d, "
+               "\"gb_per_s\": %.1f, \"bytes_per_clock_per_sm\": %.1f}\n",
+               cases[c].src, kRing, bytes / (best * 1e-3) / 1e9,
+               double(cases[c].tiles) * kStageBytes / median(h));
+      cudaEventDestroy(a);
+      cudaEventDestroy(b);
+    }
+    if (buf) cudaFree(buf);
   }
 
   const cudaError_t e = cudaGetLastError();

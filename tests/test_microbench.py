@@ -1,7 +1,8 @@
 """The sm_103a microbenchmarks: they build without a GPU, and on a GB300 they
 report the rates the kernels' design relies on (one 128x128x16 MMA per ~64
 cycles, twice that at N = 256; the prefill MMA warp's step sequence above its
-2048 MMA cycles)."""
+2048 MMA cycles; TMEM load/store bandwidth; a TMA stage ring that streams HBM
+near the copy bandwidth and L2 well above it)."""
 import os
 import subprocess
 
@@ -31,3 +32,13 @@ def test_microbench_rates():
     assert step["cycles_per_step_waits_x4"] > step["cycles_per_step"]
     (ex2,) = [r for r in recs if r["bench"] == "ex2_rate"]
     assert ex2["results_per_clock_per_sm"] > 0
+    tmem = {(r["op"].split()[0], r["warps"]): r["bytes_per_clock_per_sm"]
+            for r in recs if r["bench"] == "tmem_bw"}
+    assert set(tmem) == {("ld", 4), ("st", 4), ("ld", 8), ("st", 8)}
+    # 128 lanes x 4 bytes = 512 bytes per TMEM column: a softmax row pass of
+    # 128 columns must take far fewer cycles than the 2048-cycle MMA step
+    assert all(100 <= v <= 4096 for v in tmem.values()), tmem
+    assert tmem[("ld", 8)] >= tmem[("ld", 4)]
+    ring = {r["source"]: r["gb_per_s"] for r in recs if r["bench"] == "tma_ring_bw"}
+    assert 3000 <= ring["hbm"] <= 9000, ring   # measured copy peak ~6.7 TB/s
+    assert ring["l2"] > ring["hbm"], ring
