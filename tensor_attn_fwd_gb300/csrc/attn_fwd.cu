@@ -693,6 +693,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Launched as a programmatic dependent: the set-up above may overlap the end
+  // of the previous kernel in the stream; nothing is read or written in
+  // global memory before that kernel has completed and its writes are visible.
+  grid_dependency_wait();
+  grid_launch_dependents();  // the next kernel may start its own set-up
 
   // Register split: the softmax warpgroups hold a full S row; the MMA/TMA
   // warpgroup needs few.  256*kRegsSoftmax + 128*kRegsOther equals the
@@ -755,8 +760,8 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o
   p.split_stride_lse = static_cast<size_t>(B) * Hq * Sq;
   p.total_items = static_cast<int>(fwd_items_per_split(B, Hq, Hkv, Sq) * num_splits);
   const int grid = p.total_items < sm_count() ? p.total_items : sm_count();
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tmQ, tmK, tmV, p);
-  return cudaGetLastError();
+  return launch_programmatic(attn_fwd_kernel<D>, dim3(grid), dim3(kThreads), C::kSmemBytes,
+                             stream, tmQ, tmK, tmV, p);
 }
 
 }  // namespace

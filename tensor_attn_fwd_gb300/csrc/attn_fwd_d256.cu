@@ -625,6 +625,10 @@ __global__ void __launch_bounds__(kThreads256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Programmatic dependent: global memory is touched only after the previous
+  // kernel in the stream has completed (see attn_fwd_kernel).
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp < 4) {
     softmax_role256(p, bars, tmem, warp, lane);
@@ -674,8 +678,8 @@ cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, vo
   p.num_tiles = (Sq + 127) / 128;
   p.total_items = B * Hq * p.num_tiles;
   const int grid = p.total_items < sm_count() ? p.total_items : sm_count();
-  attn_fwd_d256_kernel<<<grid, kThreads256, kSmem256, stream>>>(tmQ, tmK, tmV, p);
-  return cudaGetLastError();
+  return launch_programmatic(attn_fwd_d256_kernel, dim3(grid), dim3(kThreads256), kSmem256,
+                             stream, tmQ, tmK, tmV, p);
 }
 
 }  // namespace attn

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/attn.h"
 
@@ -25,6 +26,28 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes);
 // zero).  False if the driver entry point is unavailable or rejects the map.
 bool encode_bf16_map(CUtensorMap* map, const void* base, int D, int rows, int planes,
                      int box_rows);
+
+// Launch `kernel` on `stream` as a programmatic dependent of the previous
+// kernel in the stream: its CTAs may start (and run their set-up) while that
+// kernel finishes; the kernel itself executes griddepcontrol.wait before it
+// touches global memory, so it still sees all of that kernel's writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 // Kernel launchers; arguments are already validated.  Return cudaError_t of
 // the launch.
