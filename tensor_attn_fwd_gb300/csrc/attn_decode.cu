@@ -113,6 +113,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   int* pids = reinterpret_cast<int*>(full + kWarps * kSlots);              // [warp][block]
   float* red_o = reinterpret_cast<float*>(ring);                   // [warp][row][D], after streaming
 
+  // Launched as a programmatic dependent: nothing in global memory (inputs,
+  // the sequence lengths, the partials a previous combine may still read) is
+  // touched before the previous kernel in the stream has completed.
+  grid_dependency_wait();
+
   const int split = blockIdx.x;
   const int g = blockIdx.y / head_slices;
   const int slice = blockIdx.y % head_slices;
@@ -517,12 +522,12 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, cons
   if (e != cudaSuccess) return e;
   const dim3 grid(num_splits, Hkv * head_slices, B);
   const float scale_log2 = scale * 1.4426950408889634f;
-  decode_splitkv_kernel<D><<<grid, kWarps * 32, C::kSmemBytes, stream>>>(
-      tmK, tmV, static_cast<const __nv_bfloat16*>(q), o_part, lse_part, seqlens,
+  return launch_programmatic(
+      decode_splitkv_kernel<D>, grid, dim3(kWarps * 32), C::kSmemBytes, stream, tmK, tmV,
+      static_cast<const __nv_bfloat16*>(q), o_part, lse_part, seqlens,
       paged != nullptr ? paged->block_table : nullptr, paged != nullptr ? paged->page_size : 0,
       paged != nullptr ? paged->max_pages : 0, paged != nullptr ? paged->num_pages : 0, B, Hq, Hkv,
       Sk, num_splits, head_slices, scale_log2, status);
-  return cudaGetLastError();
 }
 
 }  // namespace
