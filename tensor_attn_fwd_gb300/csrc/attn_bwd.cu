@@ -22,9 +22,12 @@
 //                 after dV has read it), so the gradient warps' dS^T(s) overlaps
 //                 dV(s) and S^T(s+1); then dK(s) once dS^T(s) is in TMEM and
 //                 dP^T(s+1), which overlap the exponentials of step s+1.
-//   dQ kernel     one CTA per 128-row query tile: S = Q K^T and dP = dO V^T
-//                 recomputed for each visible KV tile, dS written into TMEM,
-//                 dQ += dS K accumulated in TMEM.  S(s+1) is issued as soon as
+//   dQ kernel     persistent (one CTA per SM) over the 128-row query tiles,
+//                 highest first: S = Q K^T and dP = dO V^T recomputed for each
+//                 visible KV tile, dS written into TMEM, dQ += dS K accumulated
+//                 in one of two TMEM buffers (a tile's epilogue overlaps the
+//                 next tile's products; its Q and dO load once the current
+//                 tile's last S and dP are done).  S(s+1) is issued as soon as
 //                 the gradient warps have read S(s), so it overlaps their work
 //                 on step s; K and V stream through separate rings (K is
 //                 needed until dQ(s), V only until dP(s)).
@@ -90,6 +93,8 @@ struct BwdBars {
   uint64_t ds_full;   // dS (or dS^T) written
   uint64_t acc_full;  // all accumulating MMAs have completed
   uint64_t mma_done;
+  // persistent dQ kernel: Q/dO buffer reusable; dQ accumulator b complete / read out
+  uint64_t q_empty, acc_full2[2], acc_free[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -555,6 +560,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ------------------------------------------------------------------ dQ
+// Persistent: min(#query tiles, #SMs) CTAs, each walking the query tiles
+// (highest tile first, i.e. longest under a causal mask) in the order c,
+// 2G-1-c, 2G+c, ... (G CTAs), which balances a descending cost list.  Across
+// its tiles a CTA keeps one TMEM allocation and its barrier phases; the next
+// tile's Q and dO load as soon as the current tile's last S and dP products
+// are done, and the dQ accumulator alternates between two TMEM buffers so that
+// one tile's epilogue overlaps the next tile's products.
+__device__ __forceinline__ int dq_tile_index(int round, int cta, int grid) {
+  return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -571,17 +587,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdBars* bars = reinterpret_cast<BwdBars*>(sV + kVStages * C::kTile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Work: query tile m of head (b, h); CTAs are numbered m-major, highest m
-  // (largest work under a causal mask) first.
+  // Work: query tile m of head (b, h), numbered m-major with the highest m first.
+  const int BH = p.B * p.Hq;
   const int mtiles = (p.Sq + 127) / 128;
-  const int m = mtiles - 1 - static_cast<int>(blockIdx.x / (p.B * p.Hq));
-  const int bh = blockIdx.x % (p.B * p.Hq);
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int bkv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int nsteps = kv_tiles_for(p, m);
+  const int total = BH * mtiles;
+  const int group = p.Hq / p.Hkv;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->fixed_full, 1);
+    mbar_init(&bars->fixed_full, 1);  // this tile's Q and dO have landed
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
@@ -594,7 +608,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, kGradThreads / 32);  // one arrival per gradient warp
     mbar_init(&bars->ds_full, kGradThreads / 32);
-    mbar_init(&bars->acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full2[b], 1);
+      mbar_init(&bars->acc_free[b], kGradThreads / 32);
+    }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -610,85 +627,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   bool ok = true;
 
   if (warp == kBwdLoadWarp) {
-    if (nsteps > 0) {
+    uint32_t G = 0;   // first global step of the current tile
+    uint32_t gl = 0;  // steps whose K and V copies were issued
+    int kt = 0;       // tiles with work so far (Q/dO loads issued)
+    for (int rnd = 0; ok; ++rnd) {
+      const int idx = dq_tile_index(rnd, blockIdx.x, gridDim.x);
+      if (idx >= total) break;
+      const int m = mtiles - 1 - idx / BH, bh = idx % BH;
+      const int nsteps = kv_tiles_for(p, m);
+      if (nsteps == 0) continue;
+      const int bkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / group;
+      // Q and dO of this tile once the previous tile's last S and dP are done.
+      if (kt > 0 && !(ok = __all_sync(0xffffffffu, bwd_wait(&bars->q_empty, (kt - 1) & 1, bars))))
+        break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&bars->fixed_full, 2 * C::kTile);
         load_tile<D>(sQ, &tmQ, &bars->fixed_full, 128 * m, bh);
         load_tile<D>(sDO, &tmDO, &bars->fixed_full, 128 * m, bh);
       }
       __syncwarp();
+      ++kt;
       // K(s) and V(s) in use order; K(s) is held until dQ(s), V(s) until dP(s).
       for (int s = 0; s < nsteps && ok; ++s) {
-        const int sk = s % kKStages, sv = s % kVStages;
+        const uint32_t g = G + s;
+        const int sk = g % kKStages, sv = g % kVStages;
         bool good = true;
-        if (s >= kKStages) good = bwd_wait(&bars->empty[sk], ((s / kKStages) - 1) & 1, bars);
+        if (g >= uint32_t(kKStages))
+          good = bwd_wait(&bars->empty[sk], ((g / kKStages) - 1) & 1, bars);
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars->full[sk], C::kTile);
           load_tile<D>(sK + sk * C::kTile, &tmK, &bars->full[sk], 128 * s, bkv);
         }
         __syncwarp();
-        if (s >= kVStages) good &= bwd_wait(&bars->empty_v[sv], ((s / kVStages) - 1) & 1, bars);
+        if (g >= uint32_t(kVStages))
+          good &= bwd_wait(&bars->empty_v[sv], ((g / kVStages) - 1) & 1, bars);
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars->full_v[sv], C::kTile);
           load_tile<D>(sV + sv * C::kTile, &tmV, &bars->full_v[sv], 128 * s, bkv);
         }
         __syncwarp();
+        gl = g + 1;
         ok = __all_sync(0xffffffffu, good);
       }
-      if (!ok) bwd_record(p.status);
-      for (int s = max(0, nsteps - kKStages); s < nsteps; ++s)
-        (void)mbar_wait(&bars->full[s % kKStages], (s / kKStages) & 1);
-      for (int s = max(0, nsteps - kVStages); s < nsteps; ++s)
-        (void)mbar_wait(&bars->full_v[s % kVStages], (s / kVStages) & 1);
-      (void)mbar_wait(&bars->fixed_full, 0);
+      G += nsteps;
     }
+    if (!ok) bwd_record(p.status);
+    // Every copy this warp issued lands before the CTA can exit (older copies
+    // have landed: their slots were released after their use).
+    for (uint32_t g = (gl > uint32_t(kKStages) ? gl - kKStages : 0); g < gl; ++g)
+      (void)mbar_wait(&bars->full[g % kKStages], (g / kKStages) & 1);
+    for (uint32_t g = (gl > uint32_t(kVStages) ? gl - kVStages : 0); g < gl; ++g)
+      (void)mbar_wait(&bars->full_v[g % kVStages], (g / kVStages) & 1);
+    if (kt > 0) (void)mbar_wait(&bars->fixed_full, (kt - 1) & 1);
   } else if (warp == kBwdMmaWarp) {
-    if (nsteps > 0) {
-      ok = bwd_wait_w(&bars->fixed_full, 0, bars);
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-      auto issue_s = [&](int s) -> bool {  // S = Q K^T; this lane's wait outcome
-        const int sk = s % kKStages;
-        const bool got = bwd_wait(&bars->full[sk], (s / kKStages) & 1, bars);
-        mma_ss_tile<D>(tmem, C::kColS, q_addr, k_base + sk * C::kTile);
-        tc_commit_w(&bars->s_full);
-        return got;
-      };
-      auto issue_dp = [&](int s) -> bool {  // dP = dO V^T; V(s) is free afterwards
-        const int sv = s % kVStages;
-        const bool got = bwd_wait(&bars->full_v[sv], (s / kVStages) & 1, bars);
-        mma_ss_tile<D>(tmem, C::kColDP, do_addr, v_base + sv * C::kTile);
-        tc_commit_w(&bars->dp_full);
-        tc_commit_w(&bars->empty_v[sv]);
-        return got;
-      };
-      if (ok) {
-        bool got = issue_s(0);
-        got &= issue_dp(0);
-        ok = __all_sync(0xffffffffu, got);
-      }
-      bool good = true;  // one vote after the loop, as in the dK/dV kernel
-      for (int s = 0; s < nsteps && ok; ++s) {
-        // S(s+1) as soon as the gradient warps have read S(s) ...
+    const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
+    const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+    auto issue_s = [&](uint32_t g) -> bool {  // S = Q K^T; this lane's wait outcome
+      const int sk = g % kKStages;
+      const bool got = bwd_wait(&bars->full[sk], (g / kKStages) & 1, bars);
+      mma_ss_tile<D>(tmem, C::kColS, q_addr, k_base + sk * C::kTile);
+      tc_commit_w(&bars->s_full);
+      return got;
+    };
+    auto issue_dp = [&](uint32_t g) -> bool {  // dP = dO V^T; V(g) is free afterwards
+      const int sv = g % kVStages;
+      const bool got = bwd_wait(&bars->full_v[sv], (g / kVStages) & 1, bars);
+      mma_ss_tile<D>(tmem, C::kColDP, do_addr, v_base + sv * C::kTile);
+      tc_commit_w(&bars->dp_full);
+      tc_commit_w(&bars->empty_v[sv]);
+      return got;
+    };
+    uint32_t G = 0;  // first global step of the current tile
+    int kt = 0;      // tiles with work so far
+    bool good = true;  // one vote per tile, as in the dK/dV kernel's loop
+    for (int rnd = 0; ok; ++rnd) {
+      const int idx = dq_tile_index(rnd, blockIdx.x, gridDim.x);
+      if (idx >= total) break;
+      const int nsteps = kv_tiles_for(p, mtiles - 1 - idx / BH);
+      if (nsteps == 0) continue;
+      const int buf = kt & 1;
+      const uint32_t acc_col = buf ? C::kColA1 : C::kColA0;
+      good &= bwd_wait(&bars->fixed_full, kt & 1, bars);  // this tile's Q and dO
+      // The epilogue of tile kt-2 has read this accumulator buffer.
+      if (kt >= 2) good &= bwd_wait(&bars->acc_free[buf], ((kt >> 1) - 1) & 1, bars);
+      // S(G) overwrites the S columns once the previous step's S has been read.
+      if (G > 0) good &= bwd_wait(&bars->p_ready, (G - 1) & 1, bars);
+      tc_fence_after();
+      good &= issue_s(G);
+      good &= issue_dp(G);
+      if (nsteps == 1) tc_commit_w(&bars->q_empty);  // last S and dP of the tile issued
+      for (int s = 0; s < nsteps; ++s) {
+        const uint32_t g = G + s;
+        // S(g+1) as soon as the gradient warps have read S(g) ...
         if (s + 1 < nsteps) {
-          good &= bwd_wait(&bars->p_ready, s & 1, bars);
+          good &= bwd_wait(&bars->p_ready, g & 1, bars);
           tc_fence_after();
-          good &= issue_s(s + 1);
+          good &= issue_s(g + 1);
         }
-        // ... dQ += dS K once dS(s) is in TMEM (K MN-major: its rows are the K dim) ...
-        good &= bwd_wait(&bars->ds_full, s & 1, bars);
+        // ... dQ += dS K once dS(g) is in TMEM (K MN-major: its rows are the K dim) ...
+        good &= bwd_wait(&bars->ds_full, g & 1, bars);
         tc_fence_after();
-        mma_ts_acc<D>(tmem, C::kColA0, C::kColDP, k_base + (s % kKStages) * C::kTile, s == 0);
-        tc_commit_w(&bars->empty[s % kKStages]);
-        // ... then dP(s+1), which overwrites dS(s) after dQ has read it.
-        if (s + 1 < nsteps) good &= issue_dp(s + 1);
+        mma_ts_acc<D>(tmem, acc_col, C::kColDP, k_base + (g % kKStages) * C::kTile, s == 0);
+        tc_commit_w(&bars->empty[g % kKStages]);
+        // ... then dP(g+1), which overwrites dS(g) after dQ has read it.  After
+        // the tile's last dP, Q and dO may be replaced by the next tile's.
+        if (s + 1 < nsteps) {
+          good &= issue_dp(g + 1);
+          if (s + 2 == nsteps) tc_commit_w(&bars->q_empty);
+        }
       }
-      ok = ok && __all_sync(0xffffffffu, good);
-      if (ok) tc_commit_w(&bars->acc_full);
-      if (!ok) bwd_record(p.status);
-      tc_commit_w(&bars->mma_done);
-      (void)mbar_wait(&bars->mma_done, 0);
+      tc_commit_w(&bars->acc_full2[buf]);
+      G += nsteps;
+      ++kt;
+      ok = __all_sync(0xffffffffu, good);
     }
+    if (!ok) bwd_record(p.status);
+    // Every MMA this warp issued completes before TMEM is released.
+    tc_commit_w(&bars->mma_done);
+    (void)mbar_wait(&bars->mma_done, 0);
   } else {
     // Gradient warps: thread r owns query row 128m + r (TMEM lane r); warpgroup
     // `half` handles keys [64*half, 64*half + 64) of each tile.
@@ -696,81 +752,97 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = warp >> 2;
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    const int row = 128 * m + r;
-    const bool row_valid = row < p.Sq;
-    const float lse2 = row_valid ? __ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e
-                                 : 0.f;
-    const float dlt = row_valid ? __ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
     const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
-    const uint64_t nl2 = f2_pack(-lse2, -lse2);
-    const uint64_t ndl = f2_pack(-dlt, -dlt);
-    const int key_hi = p.causal ? min(p.Sk - 1, row + p.Sk - p.Sq) : p.Sk - 1;
-    for (int s = 0; s < nsteps && ok; ++s) {
-      ok = __all_sync(0xffffffffu, bwd_wait(&bars->s_full, s & 1, bars));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tmem + lane_addr + C::kColS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      tmem_ld32(tmem + lane_addr + C::kColS + 64 * half + 32,
-                *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      // S(s) is in registers: its columns may be overwritten by S(s+1).
-      tc_fence_before();
-      mbar_arrive_warp(&bars->p_ready);
-      // Keys 128s + 64*half + e are visible for e < n_vis (causal limit, Sk).
-      const int n_vis = row_valid ? min(max(key_hi - (128 * s + 64 * half) + 1, 0), 64) : 0;
-      const bool need_mask = __any_sync(0xffffffffu, n_vis < 64);
-      float pv[64];
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2, nl2),
-                  x0, x1);
-        float p0 = ex2(x0), p1 = ex2(x1);
-        if (need_mask) {
-          p0 = e < n_vis ? p0 : 0.f;
-          p1 = e + 1 < n_vis ? p1 : 0.f;
-        }
-        pv[e] = p0;
-        pv[e + 1] = p1;
-      }
-      ok = __all_sync(0xffffffffu, bwd_wait(&bars->dp_full, s & 1, bars));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t dr[32];
-        tmem_ld32(tmem + lane_addr + C::kColDP + 64 * half + 32 * cc, dr);
-        uint32_t dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(pv[32 * cc + e], pv[32 * cc + e + 1]),
-                           f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                  ndl)),
-                    d0, d1);
-          dk[e >> 1] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(tmem + lane_addr + C::kColDP + 64 * half + 16 * cc, dk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive_warp(&bars->ds_full);
-    }
-    if (ok) {
+    const size_t q_bytes = static_cast<size_t>(p.B) * p.Hq * p.Sq * D * sizeof(float);
+    uint32_t G = 0;  // first global step of the current tile
+    int kt = 0;      // tiles with work so far
+    for (int rnd = 0; ok; ++rnd) {
+      const int idx = dq_tile_index(rnd, blockIdx.x, gridDim.x);
+      if (idx >= total) break;
+      const int m = mtiles - 1 - idx / BH, bh = idx % BH;
+      const int nsteps = kv_tiles_for(p, m);
+      const int row = 128 * m + r;
+      const bool row_valid = row < p.Sq;
       float* dq_row = p.out0 + (static_cast<size_t>(bh) * p.Sq + row) * D;
-      const size_t q_bytes = static_cast<size_t>(p.B) * p.Hq * p.Sq * D * sizeof(float);
       if (nsteps == 0) {
+        // No key is visible to these rows: their gradient is zero.
         if (row_valid && store_in_bounds(dq_row, D * 4, p.out0, q_bytes, p.status))
           for (int c = half * D / 2; c < (half + 1) * D / 2; c += 4)
             *reinterpret_cast<float4*>(dq_row + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        ok = __all_sync(0xffffffffu, bwd_wait(&bars->acc_full, 0, bars));
-        if (ok) {
-          tc_fence_after();
-          store_acc_row<D>(tmem + lane_addr + C::kColA0, dq_row, p.scale, row_valid,
-                           half * D / 2, (half + 1) * D / 2, lane, p.out0, q_bytes, p.status);
-        }
+        continue;
       }
+      const float lse2 = row_valid ? __ldg(p.lse + static_cast<size_t>(bh) * p.Sq + row) * kLog2e
+                                   : 0.f;
+      const float dlt = row_valid ? __ldg(p.delta + static_cast<size_t>(bh) * p.Sq + row) : 0.f;
+      const uint64_t nl2 = f2_pack(-lse2, -lse2);
+      const uint64_t ndl = f2_pack(-dlt, -dlt);
+      const int key_hi = p.causal ? min(p.Sk - 1, row + p.Sk - p.Sq) : p.Sk - 1;
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const uint32_t g = G + s;
+        ok = __all_sync(0xffffffffu, bwd_wait(&bars->s_full, g & 1, bars));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_addr + C::kColS + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tmem + lane_addr + C::kColS + 64 * half + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        // S(g) is in registers: its columns may be overwritten by S(g+1).
+        tc_fence_before();
+        mbar_arrive_warp(&bars->p_ready);
+        // Keys 128s + 64*half + e are visible for e < n_vis (causal limit, Sk).
+        const int n_vis = row_valid ? min(max(key_hi - (128 * s + 64 * half) + 1, 0), 64) : 0;
+        const bool need_mask = __any_sync(0xffffffffu, n_vis < 64);
+        float pv[64];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2, nl2),
+                    x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
+          if (need_mask) {
+            p0 = e < n_vis ? p0 : 0.f;
+            p1 = e + 1 < n_vis ? p1 : 0.f;
+          }
+          pv[e] = p0;
+          pv[e + 1] = p1;
+        }
+        ok = __all_sync(0xffffffffu, bwd_wait(&bars->dp_full, g & 1, bars));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t dr[32];
+          tmem_ld32(tmem + lane_addr + C::kColDP + 64 * half + 32 * cc, dr);
+          uint32_t dk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(pv[32 * cc + e], pv[32 * cc + e + 1]),
+                             f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                    ndl)),
+                      d0, d1);
+            dk[e >> 1] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tmem + lane_addr + C::kColDP + 64 * half + 16 * cc, dk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(&bars->ds_full);
+      }
+      if (!ok) break;
+      // Epilogue: dQ * scale from this tile's accumulator buffer, which the
+      // MMA warp may reuse for tile kt+2 once every gradient warp has read it.
+      const int buf = kt & 1;
+      ok = __all_sync(0xffffffffu, bwd_wait(&bars->acc_full2[buf], (kt >> 1) & 1, bars));
+      if (!ok) break;
+      tc_fence_after();
+      store_acc_row<D>(tmem + lane_addr + (buf ? C::kColA1 : C::kColA0), dq_row, p.scale,
+                       row_valid, half * D / 2, (half + 1) * D / 2, lane, p.out0, q_bytes,
+                       p.status);
+      tc_fence_before();
+      mbar_arrive_warp(&bars->acc_free[buf]);
+      G += nsteps;
+      ++kt;
     }
     if (!ok) bwd_record(p.status);
   }
@@ -826,7 +898,8 @@ cudaError_t launch_bwd_impl(const void* q, const void* k, const void* v, const f
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.out0 = dq;
   p.out1 = nullptr;
-  const int q_ctas = B * Hq * ((Sq + 127) / 128);
+  const int q_tiles = B * Hq * ((Sq + 127) / 128);
+  const int q_ctas = q_tiles < sm_count() ? q_tiles : sm_count();
   bwd_dq_kernel<D><<<q_ctas, kBwdThreads, C::kSmemDq, stream>>>(tmQ, tmK, tmV, tmDO, p);
   return cudaGetLastError();
 }
