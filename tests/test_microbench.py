@@ -25,6 +25,8 @@ def test_microbench_rates():
     assert 50 <= mma["SS M128 N128 K16"] <= 90
     assert 100 <= mma["SS M128 N256 K16"] <= 180
     assert 50 <= mma["TS M128 N128 K16"] <= 90
+    # M = 64 does a quarter of the N = 256, M = 128 work but takes longer than half
+    assert 64 <= mma["SS M64 N256 K16"] <= 300
     (wait,) = [r for r in recs if r["bench"] == "wait_latency"]
     assert 5 <= wait["cycles_per_try_wait"] <= 500
     (step,) = [r for r in recs if r["bench"] == "step_sequence"]
