@@ -109,10 +109,12 @@ ATTN_API int attn_fwd_splitkv(const void *q, const void *k, const void *v, float
  * this library, not part of the method).  The prefill's work items are pairs
  * of 128-row query tiles: B * Hq * ceil(Sq / 256) of them, or B * Hq / 2 when
  * Sq <= 128 and Hq / Hkv is even (two query heads of one KV group share an
- * item).  With the items already filling at least 80 % of the SMs, 1 (use
- * attn_fwd); otherwise the largest count that still runs every item in one
- * round on the SMs (floor(SMs / items)), with at least four 128-key tiles per
- * split.  Always 1 for D = 256.  Host-only: launches nothing.
+ * item).  With the items already filling at least 80 % of the SMs, or with
+ * Sk <= 2 * Sq and fewer than 16 128-key tiles (the combine would cost more
+ * than the split saves), 1 (use attn_fwd); otherwise the largest count that
+ * still runs every item in one round on the SMs (floor(SMs / items)), with at
+ * least four 128-key tiles per split.  Always 1 for D = 256.  Host-only:
+ * launches nothing.
  *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0,
  *   ATTN_ERR_CUDA if the device cannot be queried.
  */

@@ -228,12 +228,19 @@ int attn_fwd_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int D, int* num_
   if (D == 64 || D == 128) {
     // Work items without splitting (two 128-row query tiles each).
     const long long base = fwd_items_per_split(B, Hq, Hkv, Sq);
-    if (base * 5 < static_cast<long long>(n_sm) * 4) {
+    const long long kv_tiles = (Sk + 127) / 128;
+    // Splitting pays when it removes more KV steps from every item than the
+    // combine and the partials cost: a cache long against the chunk
+    // (Sk > 2 Sq) or at least 16 KV tiles.  Measured counter-examples: causal
+    // or not, B1 H16 S1024 D64 (one pass 14.0 us, 2 splits 14.8) and B1 Hq32
+    // Hkv8 Sq512 Sk1024 (16.2 vs 18.2).
+    const bool worth = Sk > 2ll * Sq || kv_tiles >= 16;
+    if (worth && base * 5 < static_cast<long long>(n_sm) * 4) {
       // Too few to fill the GPU: as many splits as still fit every item in one
       // round on the SMs (a second round would cost as much as it saves), each
       // split keeping at least four 128-key tiles.
       ns = n_sm / base > 1 ? n_sm / base : 1;
-      const long long cap = (Sk + 127) / 128 / 4 > 1 ? (Sk + 127) / 128 / 4 : 1;
+      const long long cap = kv_tiles / 4 > 1 ? kv_tiles / 4 : 1;
       if (ns > cap) ns = cap;
     }
   }

@@ -91,6 +91,12 @@ def test_auto_split_count():
     # Enough items to fill the GPU: one pass.
     assert attn.attn_fwd_num_splits(4, 32, 8, 8192, 8192, 128) == 1
     assert attn.attn_fwd_num_splits(1, 4, 2, 200, 8192, 256) == 1
+    # Short caches against comparable chunks: the combine would cost more.
+    assert attn.attn_fwd_num_splits(1, 16, 16, 1024, 1024, 64) == 1
+    assert attn.attn_fwd_num_splits(1, 32, 8, 512, 1024, 128) == 1
+    # ... but a long cache, or 16+ KV tiles, still splits.
+    assert attn.attn_fwd_num_splits(1, 32, 8, 256, 1024, 128) > 1
+    assert attn.attn_fwd_num_splits(1, 8, 8, 2048, 2048, 128) > 1
     q, k, v = make_qkv(1, 4, 2, 200, 3000, 128, seed=11)
     o, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits="auto")
     torch.cuda.synchronize()
