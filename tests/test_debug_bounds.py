@@ -89,3 +89,25 @@ def test_debug_build_backward_matches_release(dbg, B, Hq, Hkv, S, D, causal):
     assert dbg.attn_debug_status(None) == attn.ATTN_OK
     for got, want in zip((dq, dk, dv), ref):
         assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("i", range(0, 120, 4))
+def test_debug_build_random_forward_shapes(dbg, i):
+    # Every fourth shape of the random sweep (odd lengths, Sq > Sk causal, all
+    # head dimensions and groupings), one pass, fp32 or bf16 output.
+    from test_fuzz import fwd_case
+    c = fwd_case(i)
+    q, k, v = (t.cuda() for t in make_qkv(c["B"], c["Hq"], c["Hkv"], c["Sq"], c["Sk"], c["D"],
+                                          c["seed"], q_std=c["std"], k_std=c["std"]))
+    bf16o = c["out"] == "bf16"
+    fwd = attn.attn_fwd_bf16o if bf16o else attn.attn_fwd
+    o_ref, lse_ref = fwd(q, k, v, causal=c["causal"], scale=c["scale"])
+    o = torch.full_like(o_ref, 3.0)
+    lse = torch.full_like(lse_ref, 3.0)
+    fn = dbg.attn_fwd_bf16o if bf16o else dbg.attn_fwd
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), c["B"],
+            c["Hq"], c["Hkv"], c["Sq"], c["Sk"], c["D"], int(c["causal"]), c["scale"],
+            torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK
+    assert dbg.attn_debug_status(None) == attn.ATTN_OK, c
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), c
