@@ -148,18 +148,23 @@ __device__ __forceinline__ int tile_bh(const FwdParams& p, const Item& it, int t
 }
 
 // Split-major order: every item of split 0 (the longest) first, then split 1, ...;
-// within a split, highest query rows first.  KV_MAJOR (a separate
-// instantiation, so that the default order's code is compiled as it was; a
-// runtime branch here cost the causal launches ~1 %) walks a split KV head by
-// KV head instead: its query heads fastest, then its row pairs, so that the
-// items sharing a KV head's K/V run at the same time and find them in L2.  The
-// host takes it only without the causal mask (every item then has the same
-// length, so the order costs no balance) and when a KV head has at most 32
-// items; then the default order spreads them over as many rounds and re-reads
-// K/V from DRAM when all K/V exceed L2 (multi-head B8 H16 S2048: +10 %).  With
-// more (B1 H16 S16384, GQA B2 Hq32 S8192) each round already streams every KV
-// head's K/V in step across several CTAs, and KV_MAJOR measured 1.5-2.5 % slower.
-template <bool KV_MAJOR>
+// within a split one of two orders, each its own instantiation of the kernel
+// (a runtime branch in this shared lookup cost the default order ~1 % on
+// causal launches whose path had not changed):
+//   ORDER 0  highest query rows first (longest first under the causal mask).
+//   ORDER 1  KV head by KV head: its query heads fastest, then its row pairs, so
+//            that the items sharing a KV head's K/V run at the same time and
+//            find them in L2.  The host (fwd_item_order) takes it only without
+//            the causal mask (every item then has the same length, so the order
+//            costs no balance) and when a KV head has at most 32 items; then
+//            ORDER 0 spreads them over as many rounds and re-reads K/V from DRAM
+//            once all K/V exceed L2 (multi-head B8 H16 S2048: +10 %).  With more
+//            (B1 H16 S16384, GQA B2 Hq32 S8192) each round already streams every
+//            KV head's K/V in step across several CTAs, and ORDER 1 measured
+//            1.5-2.5 % slower.  Under the causal mask, chunking the KV heads so
+//            that the heads in flight stay in L2 (the D = 256 kernel's ORDER 2)
+//            measured -3 to +3 % here, so causal launches keep ORDER 0.
+template <int ORDER>
 __device__ __forceinline__ Item get_item(const FwdParams& p, int idx) {
   const int BH = p.B * p.Hq;
   Item it;
@@ -168,7 +173,7 @@ __device__ __forceinline__ Item get_item(const FwdParams& p, int idx) {
     it.split = idx / per_split;
     it.bh = 2 * (idx % per_split);
     it.q_row0 = 0;
-  } else if (!KV_MAJOR) {
+  } else if (ORDER == 0) {
     const int per_split = BH * p.num_pairs;
     it.split = idx / per_split;
     const int r = idx % per_split;
@@ -225,7 +230,7 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* 
 // elect.sync, so the warp reconverges by itself.
 
 // ------------------------------------------------------------------ producer
-template <int D, bool KV_MAJOR>
+template <int D, int ORDER>
 __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                           const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* bars) {
   using C = Cfg<D>;
@@ -240,7 +245,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
-    const Item it = get_item<KV_MAJOR>(p, idx);
+    const Item it = get_item<ORDER>(p, idx);
     const int n = max(it.n[0], it.n[1]);  // end of the item's KV tiles
     if (n <= it.j0) continue;
     const int b = it.bh / p.Hq, h = it.bh % p.Hq;  // both tiles' KV head
@@ -321,7 +326,7 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, bool KV_MAJOR>
+template <int D, int ORDER>
 __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* bars,
                          uint32_t tmem) {
   using C = Cfg<D>;
@@ -384,7 +389,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
-    const Item it = get_item<KV_MAJOR>(p, idx);
+    const Item it = get_item<ORDER>(p, idx);
     const int n = max(it.n[0], it.n[1]);  // end of the item's KV tiles
     if (n <= it.j0) continue;
     if (!(ok = wait_warp(&bars->q_full, q_ctr & 1, bars))) break;
@@ -450,7 +455,7 @@ __device__ void mma_role(const FwdParams& p, uint8_t* sQ, uint8_t* sKV, Bars* ba
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, bool KV_MAJOR>
+template <int D, int ORDER>
 __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int warp, int lane) {
   using C = Cfg<D>;
   const int t = warp >> 2;
@@ -466,7 +471,7 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
-    const Item it = get_item<KV_MAJOR>(p, idx);
+    const Item it = get_item<ORDER>(p, idx);
     // This warpgroup's tile (t is a runtime value: select, do not index, so the
     // item stays in registers).
     const int nt = t ? it.n[1] : it.n[0];  // end of this tile's KV tiles in the split
@@ -668,7 +673,7 @@ __device__ void softmax_role(const FwdParams& p, Bars* bars, uint32_t tmem, int 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool KV_MAJOR>
+template <int D, int ORDER>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -724,13 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // launch allocation of 384 threads x 168 registers (checked at build time).
   if (warp < 8) {
     setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, KV_MAJOR>(p, bars, tmem, warp, lane);
+    softmax_role<D, ORDER>(p, bars, tmem, warp, lane);
   } else {
     setmaxnreg_dec<kRegsOther>();
     if (warp == kMmaWarp) {
-      mma_role<D, KV_MAJOR>(p, sQ, sKV, bars, tmem);
+      mma_role<D, ORDER>(p, sQ, sKV, bars, tmem);
     } else if (warp == kLoadWarp) {
-      load_role<D, KV_MAJOR>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+      load_role<D, ORDER>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
     }
   }
 
@@ -753,10 +758,9 @@ cudaError_t launch_fwd_impl(const void* q, const void* k, const void* v, void* o
   if (!encode_bf16_map(&tmQ, q, D, Sq, B * Hq, 128) || !encode_bf16_map(&tmK, k, D, Sk, B * Hkv, 128) ||
       !encode_bf16_map(&tmV, v, D, Sk, B * Hkv, 128))
     return cudaErrorInvalidValue;
-  // KV-head-major item order: see get_item.
-  const bool kv_major = !causal && !fwd_head_pairs(Hq, Hkv, Sq) &&
-                        (Hq / Hkv) * ((Sq + kRowsPerItem - 1) / kRowsPerItem) <= 32;
-  auto kernel = kv_major ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
+  // Item order: see get_item.
+  const int order = fwd_item_order(B, Hq, Hkv, Sq, Sk, D, causal);
+  auto kernel = order == 1 ? attn_fwd_kernel<D, 1> : attn_fwd_kernel<D, 0>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel),
                                    static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;

@@ -89,6 +89,7 @@ struct Params256 {
   float scale_log2;
   int num_tiles;    // ceil(Sq / 128)
   int total_items;  // B * Hq * num_tiles
+  int kv_chunk;     // ORDER 2: KV heads per chunk
 };
 
 struct Item256 {
@@ -115,21 +116,37 @@ __device__ __forceinline__ int item_idx(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
-// KV_MAJOR (a separate instantiation, so that the default order's code is
-// compiled as it was) walks the tiles KV head by KV head instead: its query
-// heads fastest, then its row tiles, so that the items sharing a KV head's K/V
-// run at the same time and read them from L2.  The host takes it for every
-// launch without the causal mask (every item then has the same length, so the
-// order costs no balance): with one query tile per CTA this kernel streams twice
-// the K/V per tensor cycle of the D <= 128 kernel, and the order gained on every
-// measured shape (multi-head B8 H16 S2048 +37 %, GQA B4 Hq32 Hkv8 S4096 +5 %).
-template <bool KV_MAJOR>
+// Within the launch one of three orders, each its own instantiation (so that
+// the default order's code is compiled as it was):
+//   ORDER 0  highest query tiles first (longest first under the causal mask).
+//   ORDER 1  KV head by KV head (its query heads fastest, then its row tiles),
+//            so that the items sharing a KV head's K/V run at the same time and
+//            read them from L2; for every launch without the causal mask (every
+//            item then has the same length, so the order costs no balance).  With
+//            one query tile per CTA this kernel streams twice the K/V per tensor
+//            cycle of the D <= 128 kernel, and the order gained on every measured
+//            shape (multi-head B8 H16 S2048 +43 %, GQA B4 Hq32 Hkv8 S4096 +9 %).
+//   ORDER 2  chunks of kv_chunk KV heads (48 MB of K/V), each in ORDER 0: under
+//            the causal mask when all K/V exceed twice that and Sq <= 4096, so
+//            that the heads in flight keep their K/V in L2 while longest first
+//            within a chunk keeps the CTAs balanced (multi-head B8 H16 S2048
+//            +29 %, B4 H16 S4096 +8 %, GQA B4 Hq32 Hkv8 S4096 +6.5 %).  At
+//            S = 8192 the chunks' longest-first lists no longer balance across
+//            the CTAs (multi-head D = 128 B4 H32 S8192: -5 to -8 %).
+template <int ORDER>
 __device__ __forceinline__ Item256 item_at(const Params256& p, int idx) {
   const int BH = p.B * p.Hq;
   Item256 it;
-  if (!KV_MAJOR) {
+  if (ORDER == 0) {
     it.bh = idx % BH;
     it.row0 = (p.num_tiles - 1 - idx / BH) * 128;
+  } else if (ORDER == 2) {
+    const int group = p.Hq / p.Hkv;
+    const int full = p.kv_chunk * group * p.num_tiles;  // items of a full chunk
+    const int c = idx / full, rc = idx % full;
+    const int qh_in = min(p.kv_chunk, p.B * p.Hkv - c * p.kv_chunk) * group;
+    it.bh = c * p.kv_chunk * group + rc % qh_in;  // KV heads' query heads are contiguous
+    it.row0 = (p.num_tiles - 1 - rc / qh_in) * 128;
   } else {
     const int group = p.Hq / p.Hkv;
     const int rest = idx / group;
@@ -142,13 +159,13 @@ __device__ __forceinline__ Item256 item_at(const Params256& p, int idx) {
 }
 
 // Next item of this CTA with work, starting at round r (r is advanced past it).
-template <bool KV_MAJOR>
+template <int ORDER>
 __device__ __forceinline__ bool next_work(const Params256& p, int& r, Item256& it) {
   while (true) {
     const int idx = item_idx(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) return false;
     ++r;
-    it = item_at<KV_MAJOR>(p, idx);
+    it = item_at<ORDER>(p, idx);
     if (it.n > 0) return true;
   }
 }
@@ -209,7 +226,7 @@ __device__ __forceinline__ bool load_half(const CUtensorMap* map, int half, int 
   return got;  // this lane's outcome
 }
 
-template <bool KV_MAJOR>
+template <int ORDER>
 __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                              const CUtensorMap* tmV, const Params256& p, uint8_t* sQ,
                              uint8_t* sKV, Bars256* bars) {
@@ -219,7 +236,7 @@ __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   bool ok = true;
   int r = 0;
   Item256 it;
-  if (!next_work<KV_MAJOR>(p, r, it)) return;
+  if (!next_work<ORDER>(p, r, it)) return;
   auto load_q_k0 = [&](const Item256& x) -> bool {
     if (q_ctr > 0 && !wait_bar_w(&bars->q_empty, (q_ctr - 1) & 1, bars)) return false;
     if (elect_one()) {
@@ -246,7 +263,7 @@ __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         g &= load_half(tmK, 0, (j + 1) * 128, bkv, sKV, bars, ring);
         g &= load_half(tmK, 1, (j + 1) * 128, bkv, sKV, bars, ring);
       } else {
-        have_next = next_work<KV_MAJOR>(p, r, nxt);
+        have_next = next_work<ORDER>(p, r, nxt);
         if (have_next) g &= load_q_k0(nxt);
       }
       g &= load_half(tmV, 0, j * 128, bkv, sKV, bars, ring);
@@ -265,7 +282,7 @@ __device__ void load_role256(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <bool KV_MAJOR>
+template <int ORDER>
 __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars256* bars,
                             uint32_t tmem) {
   constexpr uint64_t kDescK = sdesc_sw128(0, 16, 1024);    // Q and K: K-major
@@ -317,7 +334,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
 
   int r = 0;
   Item256 it;
-  if (!next_work<KV_MAJOR>(p, r, it)) return;
+  if (!next_work<ORDER>(p, r, it)) return;
   if (!(ok = wait_bar_w(&bars->q_full, q_ctr & 1, bars))) goto done;
   ++q_ctr;
   if (!(ok = __all_sync(0xffffffffu, issue_s()))) goto done;
@@ -332,7 +349,7 @@ __device__ void mma_role256(const Params256& p, uint8_t* sQ, uint8_t* sKV, Bars2
         good &= issue_s();
         if (j + 2 == it.n) tc_commit_w(&bars->q_empty);  // the item's last S is issued
       } else {
-        have_next = next_work<KV_MAJOR>(p, r, nxt);
+        have_next = next_work<ORDER>(p, r, nxt);
         if (have_next) {
           if (!(ok = wait_bar_w(&bars->q_full, q_ctr & 1, bars))) goto done;
           ++q_ctr;
@@ -397,7 +414,7 @@ done:
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-template <bool KV_MAJOR>
+template <int ORDER>
 __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem, int warp,
                                 int lane) {
   const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
@@ -409,7 +426,7 @@ __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem
   for (int r = 0; ok; ++r) {
     const int idx = item_idx(r, blockIdx.x, gridDim.x);
     if (idx >= p.total_items) break;
-    const Item256 it = item_at<KV_MAJOR>(p, idx);
+    const Item256 it = item_at<ORDER>(p, idx);
     const int row = it.row0 + warp * 32 + lane;
     const bool row_valid = row < p.Sq;
     const size_t o_off = (static_cast<size_t>(it.bh) * p.Sq + row) * kD;
@@ -603,7 +620,7 @@ __device__ void softmax_role256(const Params256& p, Bars256* bars, uint32_t tmem
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool KV_MAJOR>
+template <int ORDER>
 __global__ void __launch_bounds__(kThreads256, 1)
     attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -654,11 +671,11 @@ __global__ void __launch_bounds__(kThreads256, 1)
   grid_launch_dependents();
 
   if (warp < 4) {
-    softmax_role256<KV_MAJOR>(p, bars, tmem, warp, lane);
+    softmax_role256<ORDER>(p, bars, tmem, warp, lane);
   } else if (warp == kMmaWarp256) {
-    mma_role256<KV_MAJOR>(p, sQ, sKV, bars, tmem);
+    mma_role256<ORDER>(p, sQ, sKV, bars, tmem);
   } else if (warp == kLoadWarp256) {
-    load_role256<KV_MAJOR>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
+    load_role256<ORDER>(&tmQ, &tmK, &tmV, p, sQ, sKV, bars);
   }
 
   tc_fence_before();
@@ -680,7 +697,9 @@ cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, vo
       !encode_bf16_map(&tmK, k, kD, Sk, B * Hkv, 128) ||
       !encode_bf16_map(&tmV, v, kD, Sk, B * Hkv, 128))
     return cudaErrorInvalidValue;
-  auto kernel = causal ? attn_fwd_d256_kernel<false> : attn_fwd_d256_kernel<true>;  // item_at
+  const int order = fwd_item_order(B, Hq, Hkv, Sq, Sk, kD, causal);  // see item_at
+  auto kernel = order == 1 ? attn_fwd_d256_kernel<1>
+                           : (order == 2 ? attn_fwd_d256_kernel<2> : attn_fwd_d256_kernel<0>);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kernel),
                                    static_cast<int>(kSmem256));
   if (e != cudaSuccess) return e;
@@ -701,6 +720,7 @@ cudaError_t launch_attn_fwd_d256(const void* q, const void* k, const void* v, vo
   p.scale_log2 = scale * 1.4426950408889634f;
   p.num_tiles = (Sq + 127) / 128;
   p.total_items = B * Hq * p.num_tiles;
+  p.kv_chunk = fwd_kv_chunk(Sk, kD);
   const int grid = p.total_items < sm_count() ? p.total_items : sm_count();
   return launch_programmatic(kernel, dim3(grid), dim3(kThreads256), kSmem256,
                              stream, tmQ, tmK, tmV, p);

@@ -73,6 +73,36 @@ def test_d256_large_sampled():
     assert_close(o_s, lse_s, o_ref, lse_ref, "D256 S8192 sampled")
 
 
+def test_d256_chunked_order_every_row():
+    """Causal multi-head B8 H16 S2048 D256: 268 MB of K/V, so the kernel walks
+    the items in chunks of 24 KV heads (the last chunk holds 8), longest first
+    within each; every row against the oracle."""
+    B, H, S, D = 8, 16, 2048, 256
+    q, k, v = make_qkv(B, H, H, S, S, D, seed=2563)
+    scale = 1.0 / 16.0
+    o, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, scale)
+    assert_close(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "D256 chunked order")
+
+
+def test_d256_chunked_order_gqa_sampled():
+    """Causal GQA B4 Hq32 Hkv8 S4096 D256: 134 MB of K/V, chunks of 12 KV heads
+    (the last holds 8), on sampled rows (every head's edge rows included)."""
+    B, Hq, Hkv, S, D = 4, 32, 8, 4096, 256
+    q, k, v = make_qkv(B, Hq, Hkv, S, S, D, seed=2564)
+    scale = 1.0 / 16.0
+    o, lse = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    rows = sample_rows(B, Hq, S, n_random=256, seed=2565)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, scale, rows=rows.numpy())
+    o_s = o.reshape(-1, D)[rows.cuda()].cpu().numpy()
+    lse_s = lse.reshape(-1)[rows.cuda()].cpu().numpy()
+    assert_close(o_s, lse_s, o_ref, lse_ref, "D256 chunked order GQA sampled")
+
+
 def test_d256_backward_and_split_prefill_unsupported():
     """D = 256 has the one-pass forward and split-KV decode (parity in
     test_parity); the backward and the split-KV prefill report
