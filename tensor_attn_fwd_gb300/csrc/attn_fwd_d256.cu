@@ -121,11 +121,13 @@ __device__ __forceinline__ int item_idx(int round, int cta, int grid) {
 //   ORDER 0  highest query tiles first (longest first under the causal mask).
 //   ORDER 1  KV head by KV head (its query heads fastest, then its row tiles),
 //            so that the items sharing a KV head's K/V run at the same time and
-//            read them from L2; for every launch without the causal mask (every
-//            item then has the same length, so the order costs no balance).  With
-//            one query tile per CTA this kernel streams twice the K/V per tensor
-//            cycle of the D <= 128 kernel, and the order gained on every measured
-//            shape (multi-head B8 H16 S2048 +43 %, GQA B4 Hq32 Hkv8 S4096 +9 %).
+//            read them from L2; without the causal mask (every item then has
+//            the same length, so the order costs no balance) when all K/V exceed
+//            96 MB.  With one query tile per CTA this kernel streams twice the K/V
+//            per tensor cycle of the D <= 128 kernel, and the order gained on
+//            every such shape measured (multi-head B8 H16 S2048 +43 %, GQA B4
+//            Hq32 Hkv8 S4096 +9 %, B16 Hq32 Hkv8 S1024 +7 %); with K/V that fit
+//            in L2 it measured 0.6-2.3 % slower.
 //   ORDER 2  chunks of kv_chunk KV heads (48 MB of K/V), each in ORDER 0: under
 //            the causal mask when all K/V exceed twice that and Sq <= 4096, so
 //            that the heads in flight keep their K/V in L2 while longest first

@@ -78,9 +78,9 @@ inline long long fwd_items_per_split(long long B, int Hq, int Hkv, int Sq) {
 }
 
 // The prefill kernels' work-item orders (each a separate kernel instantiation):
-// 0 longest first; 1 KV head by KV head (no causal mask); 2 longest first within
-// chunks of KV heads whose K/V fit in L2 (D = 256 under the causal mask, all K/V
-// beyond that, Sq <= 4096).  Measured: see the item lookups in attn_fwd.cu and
+// 0 longest first; 1 KV head by KV head (no causal mask; at D = 256 only when all
+// K/V exceed 96 MB); 2 longest first within chunks of KV heads whose K/V fit in
+// L2 (D = 256 under the causal mask, all K/V beyond 96 MB, Sq <= 4096).  Measured: see the item lookups in attn_fwd.cu and
 // attn_fwd_d256.cu.
 constexpr long long kFwdKvChunkBytes = 48ll << 20;
 inline long long fwd_kv_head_bytes(int Sk, int D) { return 4ll * Sk * D; }  // K + V, bf16
@@ -90,12 +90,12 @@ inline int fwd_kv_chunk(int Sk, int D) {
 }
 inline int fwd_item_order(long long B, int Hq, int Hkv, int Sq, int Sk, int D, int causal) {
   if (D != 256 && fwd_head_pairs(Hq, Hkv, Sq)) return 0;
+  const bool big_kv = B * Hkv * fwd_kv_head_bytes(Sk, D) > 2 * kFwdKvChunkBytes;
   if (!causal) {
-    if (D == 256) return 1;
+    if (D == 256) return big_kv ? 1 : 0;
     return static_cast<long long>(Hq / Hkv) * ((Sq + 255) / 256) <= 32 ? 1 : 0;
   }
-  return D == 256 && Sq <= 4096 && B * Hkv * fwd_kv_head_bytes(Sk, D) > 2 * kFwdKvChunkBytes
-             ? 2 : 0;
+  return D == 256 && Sq <= 4096 && big_kv ? 2 : 0;
 }
 
 // Prefill over KV splits (D 64 or 128): split s covers KV tiles
