@@ -238,12 +238,14 @@ ATTN_API int attn_qkv_rope(const void *x, const void *w, const float *rope_table
  * current device.  The pages leave the split count to the caller; this is a
  * measured rule for this library's decode kernel, not part of the method.
  * With B * Hkv * ceil((Hq/Hkv) / 16) CTAs per split already filling at least
- * 80 % of the SMs, one split streams K/V fastest; otherwise about one CTA per
- * SM (ceil(SMs / CTAs per split); at D = 256, where a CTA takes a whole SM,
- * floor, so that they run in one wave), with at least 1024 keys per split.
+ * 80 % of the SMs, one split streams K/V fastest.  Otherwise, at D = 256
+ * (where a CTA takes a whole SM) floor(SMs / CTAs per split), so that they run
+ * in one wave; at D = 64 and 128 ceil(SMs / CTAs per split), twice that at
+ * D = 64, rounded to the nearest power of two.  Each split keeps at least 256
+ * keys when there are four or more CTAs per split, else at least 1024.
  * Host-only: launches nothing.
  *
- *   *num_splits receives the count (>= 1, <= max(1, Sk / 1024)).
+ *   *num_splits receives the count (>= 1, <= max(1, Sk / 256)).
  *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0,
  *   ATTN_ERR_CUDA if the device cannot be queried.
  */

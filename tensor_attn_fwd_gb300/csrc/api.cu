@@ -414,11 +414,30 @@ int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int D, int* num_split
   const long long base = static_cast<long long>(B) * Hkv * ((Hq / Hkv + 15) / 16);
   long long ns = 1;
   if (base * 5 < static_cast<long long>(n_sm) * 4) {
-    // Too few to stream at full bandwidth: about one CTA per SM, each split
-    // keeping at least 1024 keys.  At D = 256 a decode CTA takes a whole SM,
-    // so the CTAs must fit in one wave: floor instead of ceil.
-    ns = D == 256 ? (n_sm / base > 1 ? n_sm / base : 1) : (n_sm + base - 1) / base;
-    const long long cap = Sk / 1024 > 1 ? Sk / 1024 : 1;
+    // Too few to stream at full bandwidth.  At D = 256 a decode CTA takes a
+    // whole SM, so the CTAs must fit in one wave: floor(SMs / base).  Otherwise
+    // about one CTA per SM (two at D = 64, whose CTAs are lighter), rounded to
+    // the nearest power of two: with power-of-two caches the splits then cut the
+    // keys into whole 128-key groups (four warps x 32 keys), and the measured
+    // optimum sat there (B1 Hq32 Hkv8 Sk32768: 16 splits 27.5 us, 19 splits
+    // 28.2; B4 Hq32 Hkv4 Sk32768 D64: 16 splits 28.9, 10 splits 30.4).
+    if (D == 256) {
+      ns = n_sm / base > 1 ? n_sm / base : 1;
+    } else {
+      const long long ctas = (D == 64 ? 2ll : 1ll) * n_sm;
+      const double t = static_cast<double>((ctas + base - 1) / base);
+      ns = 1ll << std::lround(std::log2(t));
+    }
+    // Each split keeps at least 128 KB of K and V per KV head (128 keys at
+    // D = 256, 256 at D = 128, 512 at D = 64): single-sequence B1 Hq32 Hkv8 Sk4096 gets 16
+    // splits, 8.9 us against the 13.4 of an earlier 1024-key floor, and
+    // B1 Hq32 Hkv8 Sk8192 D64 16 splits (11.1 us; 32 splits 13.9).  At most 32
+    // splits, the combine's one pass over a warp of partials: with one or two
+    // CTAs per split more only lengthen the combine's serial loop over them
+    // (B1 Hq8 Hkv1 Sk16384: 64 splits 16.7 us, 32 13.4).
+    if (ns > 32) ns = 32;
+    const long long min_keys = 32768 / D;
+    const long long cap = Sk / min_keys > 1 ? Sk / min_keys : 1;
     if (ns > cap) ns = cap;
   }
   *num_splits = static_cast<int>(ns);

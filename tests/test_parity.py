@@ -291,15 +291,23 @@ def test_bf16_output(B, Hq, Hkv, Sq, Sk, D, causal):
     (64, 32, 8, 4096, 128, 1),     # 512 CTAs already fill the SMs
     (4, 32, 8, 8192, 128, None),   # 32 CTAs: several splits
     (8, 32, 4, 32768, 256, None),  # D = 256: one CTA per SM, so one wave
-    (1, 32, 8, 2048, 128, 2),      # capped at Sk / 1024
+    (1, 32, 8, 2048, 128, 8),      # capped at Sk / 256 (128 KB of K and V a split)
+    (1, 32, 8, 4096, 128, None),   # 8 CTAs a split: 152 SMs -> 16 splits
+    (4, 32, 4, 32768, 64, None),   # D = 64: two CTAs per SM
+    (1, 32, 8, 8192, 64, 16),      # D = 64: capped at Sk / 512
+    (1, 8, 1, 16384, 128, 32),     # one CTA a split: at most 32 splits
     (1, 4, 1, 500, 128, 1),        # too short to split
 ])
 def test_decode_num_splits_rule(B, Hq, Hkv, Sk, D, want):
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     ns = attn.attn_decode_num_splits(B, Hq, Hkv, Sk, D)
     base = B * Hkv * (((Hq // Hkv) + 15) // 16)
-    per_sm = max(1, n_sm // base) if D == 256 else (n_sm + base - 1) // base
-    expect = want if want is not None else min(per_sm, max(1, Sk // 1024))
+    if D == 256:
+        per_sm = max(1, n_sm // base)
+    else:
+        t = -(-(2 if D == 64 else 1) * n_sm // base)
+        per_sm = min(32, 1 << int(math.floor(math.log2(t) + 0.5)))
+    expect = want if want is not None else min(per_sm, max(1, Sk // (32768 // D)))
     assert ns == expect
     # and the default decode path uses it and matches the oracle
     q, k, v = make_qkv(B, Hq, Hkv, 1, Sk, D, seed=B + Sk)
