@@ -4,8 +4,8 @@
 runs it on the current GPU and returns its measurements as dicts:
 
 - ``mma_cycles``: cycles per tcgen05.mma (bf16 -> fp32) for M128 N128 / N256
-  K16 in SS form, M128 N128 in TS form and M64 N256 in SS form, issued back to
-  back by one warp.
+  K16 in SS form, M128 N128 in TS form, M64 N256 in SS form and M128 N64 in
+  both forms, issued back to back by one warp.
 - ``wait_latency``: cycles of a dependent mbarrier.try_wait on a completed phase.
 - ``step_sequence``: cycles per KV step of the prefill MMA warp's issue
   sequence (32 MMAs, 5 waits, 4 commits) with every barrier complete, with each

@@ -77,7 +77,8 @@ __device__ void teardown(Bars* bars, uint32_t tbase, int* status) {
 }
 
 // MODE 0: SS M128 N128 K16; 1: SS M128 N256; 2: TS M128 N128 (A from TMEM);
-// 3: SS M64 N256 (A: 64 rows of the same tile).
+// 3: SS M64 N256 (A: 64 rows of the same tile); 4: SS M128 N64; 5: TS M128 N64
+// (the D = 64 forward's PV shape).
 template <int MODE>
 __global__ void __launch_bounds__(128, 1) mma_cycles(long long* out, int iters, int* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(128, 1) mma_cycles(long long* out, int iters, 
   __shared__ uint32_t tbase;
   uint8_t* sm = setup(smem_raw, &bars, &tbase);
   if (threadIdx.x < 32) {
-    constexpr int N = (MODE == 1 || MODE == 3) ? 256 : 128;
+    constexpr int N = (MODE == 1 || MODE == 3) ? 256 : MODE >= 4 ? 64 : 128;
     constexpr int M = MODE == 3 ? 64 : 128;
     constexpr uint32_t idesc = idesc_bf16_f32(M, N, false, false);
     const uint64_t a0 = sdesc_sw128(smem_u32(sm), 16, 1024);
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(128, 1) mma_cycles(long long* out, int iters, 
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t a = a0 + ((kk * 32) >> 4), b = b0 + ((kk * 32) >> 4);
-        if (MODE == 2)
+        if (MODE == 2 || MODE == 5)
           mma_ts_w<1>(tbase, tbase + 256 + kk * 8, b, idesc);
         else
           mma_ss_w<1>(tbase, a, b, idesc);
@@ -383,13 +384,15 @@ int main() {
   bool ok = true;
 
   const int iters = 2000;
-  const char* names[4] = {"SS M128 N128 K16", "SS M128 N256 K16", "TS M128 N128 K16",
-                          "SS M64 N256 K16"};
-  for (int mode = 0; mode < 4 && ok; ++mode) {
+  const char* names[6] = {"SS M128 N128 K16", "SS M128 N256 K16", "TS M128 N128 K16",
+                          "SS M64 N256 K16",  "SS M128 N64 K16",  "TS M128 N64 K16"};
+  for (int mode = 0; mode < 6 && ok; ++mode) {
     if (mode == 0) ok = launch_cta_per_sm(mma_cycles<0>, d_out, iters, d_st, h);
     if (mode == 1) ok = launch_cta_per_sm(mma_cycles<1>, d_out, iters, d_st, h);
     if (mode == 2) ok = launch_cta_per_sm(mma_cycles<2>, d_out, iters, d_st, h);
     if (mode == 3) ok = launch_cta_per_sm(mma_cycles<3>, d_out, iters, d_st, h);
+    if (mode == 4) ok = launch_cta_per_sm(mma_cycles<4>, d_out, iters, d_st, h);
+    if (mode == 5) ok = launch_cta_per_sm(mma_cycles<5>, d_out, iters, d_st, h);
     if (ok)
       printf("{\"bench\": \"mma_cycles\", \"shape\": \"%s\", \"cycles_per_mma\": %.1f}\n",
              names[mode], median(h) / (iters * 4.0));

@@ -27,6 +27,10 @@ def test_microbench_rates():
     assert 50 <= mma["TS M128 N128 K16"] <= 90
     # M = 64 does a quarter of the N = 256, M = 128 work but takes longer than half
     assert 64 <= mma["SS M64 N256 K16"] <= 300
+    # N = 64: half the N = 128 time with A in TMEM; with both operands in shared
+    # memory the 6 KB of operands per MMA take longer than the tensor work
+    assert 25 <= mma["TS M128 N64 K16"] <= 50
+    assert mma["TS M128 N64 K16"] < mma["SS M128 N64 K16"] <= 80
     (wait,) = [r for r in recs if r["bench"] == "wait_latency"]
     assert 5 <= wait["cycles_per_try_wait"] <= 500
     (step,) = [r for r in recs if r["bench"] == "step_sequence"]
