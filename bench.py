@@ -57,8 +57,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (one pass) of
 # `bench.py --profile prefill|decode`; profiles/ holds the summary.  Reset to
 # None whenever the kernel changes until it is captured again.
-PREFILL_TRAFFIC_BYTES = 331879424 + 214474752
-DECODE_TRAFFIC_BYTES = 1074305792 + 10391552
+PREFILL_TRAFFIC_BYTES = 319545344 + 214419968
+DECODE_TRAFFIC_BYTES = 1074305024 + 10365184
 
 
 def load_peaks():
