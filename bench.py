@@ -583,7 +583,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
 
     # ---------------- parity of every timed output against the fp64 oracle
     import oracle  # test infrastructure: the check, never the product path
-    configs = {}
+    per_workload = {}
     cpu = None
     parity_ok = True
     for ci in (1, 2, 3, 4):
@@ -613,7 +613,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
         del o_ref, l_ref
         cflops = cw.flops()
         c_tf = cflops / (run["ms"] * 1e-3) / 1e12
-        configs[f"C{ci}"] = {
+        per_workload[f"C{ci}"] = {
             "workload": cw.describe(), "gpu_us": run["ms"] * 1e3, "timing": run["timing"],
             "counted_flops": cflops, "value": c_tf, "unit": "TFLOP/s",
             "frac_of_measured_bf16_peak": c_tf / peaks["bf16_tflops"], "parity": par}
@@ -637,7 +637,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
                 "partials": {k2: par_p[k2] for k2 in ("o_max_abs_err", "lse_max_err", "pass")}})
     par["pass"] = bool(par["pass"] and par_p["pass"])
     parity_ok &= par["pass"]
-    configs["C5"] = {
+    per_workload["C5"] = {
         "workload": d.describe(), "gpu_us": d_ms * 1e3,
         "timing": "split + combine, CUDA events, mean of the decode object's launches",
         "algorithmic_bytes": dbytes, "value": dbytes / (d_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -668,7 +668,7 @@ def ours_arm(args, rank, world, local_rank, dist_on):
         "qkv_rope": qkv_rope,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "configs": configs,
+        "configs": per_workload,
         "parity_ok": bool(parity_ok),
         "gpu_launches": args.steps,
         "clocks": clocks,
