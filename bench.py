@@ -397,13 +397,26 @@ def ours_arm(args, rank, world, local_rank, dist_on):
         decode_split()
         decode_combine()
 
+    fo = torch.empty_like(do)
+    fl = torch.empty_like(dl)
+    fop = torch.empty_like(op)
+    flp = torch.empty_like(lp)
+    fcnt = torch.zeros(d.B * d.Hkv * ((d.Hq // d.Hkv + 15) // 16), dtype=torch.int32,
+                       device=device)
+
+    def decode_fused():  # the same decode with the combine in the split kernel
+        attn.attn_decode_fused(dq, dk, dv, d.num_splits, d.scale, o_part=fop, lse_part=flp,
+                               o=fo, lse=fl, counters=fcnt, stream=stream)
+
     decode_both()
+    decode_fused()
     torch.cuda.synchronize()
     # K+V (1.07 GB) exceed L2 eightfold: no flush between decode steps (a flush
     # would leave dirty lines whose write-back competes with the K/V stream).
     t_both = time_launches(decode_both, args.steps, args.warmup, None, stream)
     t_split = time_launches(decode_split, args.steps, args.warmup, None, stream)
     t_comb = time_launches(decode_combine, args.steps, args.warmup, None, stream)
+    t_fused = time_launches(decode_fused, args.steps, args.warmup, None, stream)
     t_clock2 = time.time()
     c5_out = (op.cpu(), lp.cpu(), do.cpu(), dl.cpu())
     dbytes = d.algorithmic_bytes()
@@ -414,6 +427,8 @@ def ours_arm(args, rank, world, local_rank, dist_on):
         "l2": "no flush: K+V 1.07 GB > L2",
         "value": dbytes / (d_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": d_ms,
         "split_kernel_ms": d_split_ms, "combine_kernel_ms": sum(t_comb) / len(t_comb),
+        "fused_one_launch_ms": sum(t_fused) / len(t_fused),
+        "fused_equals_two_launches": bool(torch.equal(fo, do) and torch.equal(fl, dl)),
         "algorithmic_bytes": dbytes,
         "frac_of_measured_hbm": dbytes / (d_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "frac_of_nominal_8tbs": dbytes / (d_ms * 1e-3) / 1e9 / 8000.0,

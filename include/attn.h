@@ -241,11 +241,11 @@ ATTN_API int attn_qkv_rope(const void *x, const void *w, const float *rope_table
  * 80 % of the SMs, one split streams K/V fastest.  Otherwise, at D = 256
  * (where a CTA takes a whole SM) floor(SMs / CTAs per split), so that they run
  * in one wave; at D = 64 and 128 ceil(SMs / CTAs per split), twice that at
- * D = 64, rounded to the nearest power of two.  Each split keeps at least 256
- * keys when there are four or more CTAs per split, else at least 1024.
- * Host-only: launches nothing.
+ * D = 64, rounded to the nearest power of two.  At most 32 splits (the
+ * combine's one pass over a warp of partials), each keeping at least 128 KB of
+ * K and V per KV head (32768 / D keys).  Host-only: launches nothing.
  *
- *   *num_splits receives the count (>= 1, <= max(1, Sk / 256)).
+ *   *num_splits receives the count (>= 1, <= max(1, min(32, Sk / (32768 / D)))).
  *   Returns ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0,
  *   ATTN_ERR_CUDA if the device cannot be queried.
  */
@@ -263,6 +263,42 @@ ATTN_API int attn_decode_num_splits(int B, int Hq, int Hkv, int Sk, int D, int *
  */
 ATTN_API int attn_combine(const float *o_part, const float *lse_part, float *o, float *lse, int B,
                  int Hq, int D, int num_splits, void *stream);
+
+/*
+ * Decode in one launch: the split-KV partials of attn_decode_splitkv (or, with
+ * seqlens, of attn_decode_splitkv_varlen), and their log-sum-exp combine
+ * (attn_combine's formula).  Source: the same pages (FlashDecoding: per-split
+ * partials, then the reduction across splits).  The combine of each (batch, KV
+ * head, 16-query-head slice) group runs in the CTA that completes the group's
+ * last split, found with one int32 counter per group, so it overlaps the
+ * streaming of other groups and needs no second kernel.
+ *
+ *   q, k, v, B, Hq, Hkv, Sk, D, num_splits, scale, stream: as attn_decode_splitkv
+ *   seqlens   optional device int32 [B] (NULL: every sequence has Sk keys), as
+ *             attn_decode_splitkv_varlen
+ *   o [B,Hq,D], lse [B,Hq]: fp32 results, 16-byte aligned
+ *   o_part [num_splits,B,Hq,D], lse_part [num_splits,B,Hq]: fp32 workspace,
+ *             16-byte aligned; holds the partials after the call
+ *   counters  device int32 [attn_decode_fused_counters(B, Hq, Hkv)], all zero
+ *             on entry.  A call that completes without a device-side error
+ *             leaves them zero, so one zeroed array serves every later call on
+ *             the same stream.  Calls whose kernels may overlap (other streams)
+ *             need arrays of their own.  After a call that reported
+ *             ATTN_ERR_TIMEOUT (attn_debug_status), zero the array again.
+ *   Returns the argument errors of attn_decode_splitkv, and ATTN_ERR_INVALID_ARG
+ *   for NULL o, lse or counters; ATTN_ERR_MISALIGNED for an unaligned output or
+ *   counter array.
+ */
+ATTN_API int attn_decode_fused(const void *q, const void *k, const void *v, const int *seqlens,
+                               float *o, float *lse, float *o_part, float *lse_part,
+                               int *counters, int B, int Hq, int Hkv, int Sk, int D,
+                               int num_splits, float scale, void *stream);
+
+/*
+ * Number of int32 counters attn_decode_fused needs: B * Hkv * ceil((Hq/Hkv)/16).
+ * Host-only.  ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0.
+ */
+ATTN_API int attn_decode_fused_counters(int B, int Hq, int Hkv, int *count);
 
 /*
  * Attention backward: gradients of sum(dO * O) for the attn_fwd computation.

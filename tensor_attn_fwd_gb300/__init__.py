@@ -31,7 +31,7 @@ import threading
 import torch
 
 __all__ = ["AttnError", "attn_fwd", "attn_fwd_bf16o", "attn_decode_splitkv", "attn_decode_splitkv_varlen",
-           "attn_decode_splitkv_paged", "attn_combine", "decode", "decode_paged", "attn_bwd",
+           "attn_decode_splitkv_paged", "attn_combine", "attn_decode_fused", "decode", "decode_paged", "attn_bwd",
            "attn_rope_table", "attn_qkv_rope", "attn_decode_num_splits",
            "attn_status_string", "attn_debug_status", "library_path", "load_library",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
@@ -66,6 +66,8 @@ _SIGNATURES = {
                                     _int, _flt, _vp], _int),
     "attn_decode_splitkv_paged": ([_vp] * 7 + [_int] * 8 + [_flt, _vp], _int),
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
+    "attn_decode_fused": ([_vp] * 9 + [_int] * 6 + [_flt, _vp], _int),
+    "attn_decode_fused_counters": ([_int, _int, _int, ctypes.POINTER(_int)], _int),
     "attn_fwd_splitkv": ([_vp] * 5 + [_int] * 8 + [_flt, _vp], _int),
     "attn_fwd_num_splits": ([_int] * 6 + [ctypes.POINTER(_int)], _int),
     "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
@@ -487,25 +489,96 @@ def attn_decode_num_splits(B: int, Hq: int, Hkv: int, Sk: int, D: int = 128,
     return int(n.value)
 
 
+# Zeroed int32 counter arrays for attn_decode_fused, one per (device, stream):
+# a call leaves its counters zero, so calls on one stream share an array and
+# calls on different streams (which may overlap) never do.
+_counters = {}
+_counters_lock = threading.Lock()
+
+
+def _stream_counters(device: torch.device, stream, n: int) -> torch.Tensor:
+    handle = _stream_handle(stream)
+    key = (device.index, handle)
+    with _counters_lock:
+        buf = _counters.get(key)
+        if buf is None or buf.numel() < n:
+            # Zeroed on the call's own stream, so the memset precedes the kernel.
+            with torch.cuda.device(device), torch.cuda.stream(
+                    torch.cuda.ExternalStream(handle, device=device)):
+                buf = torch.zeros(max(n, 1024), dtype=torch.int32, device=device)
+            _counters[key] = buf
+    return buf
+
+
+def attn_decode_fused(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int,
+                      scale: float | None = None, seqlens: torch.Tensor | None = None,
+                      o_part: torch.Tensor | None = None, lse_part: torch.Tensor | None = None,
+                      o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      counters: torch.Tensor | None = None, stream=None):
+    """Split-KV decode and its LSE combine in one launch; returns (o [B,Hq,D], lse [B,Hq]).
+
+    The partials land in o_part [num_splits,B,Hq,D] / lse_part [num_splits,B,Hq]
+    as with attn_decode_splitkv.  ``counters`` (int32 CUDA, at least
+    attn_decode_fused_counters entries, zero) defaults to a cached zeroed array of
+    the call's stream.  With ``seqlens`` sequence b attends to its first seqlens[b] keys.
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k", k, 4)
+    _check_bf16("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    _check(Sq == 1, "decode takes one query row per head (q.shape[2] == 1)")
+    Bk, Hkv, Sk, Dk = k.shape
+    _check(Bk == B and Dk == D and tuple(v.shape) == tuple(k.shape), "q/k/v shape mismatch")
+    _check(k.device == q.device and v.device == q.device, "q/k/v must share a device")
+    seq_ptr = None
+    if seqlens is not None:
+        _check(isinstance(seqlens, torch.Tensor) and seqlens.is_cuda
+               and seqlens.dtype == torch.int32 and seqlens.is_contiguous()
+               and tuple(seqlens.shape) == (B,) and seqlens.device == q.device,
+               "seqlens must be a contiguous int32 CUDA tensor of shape [B] on q's device")
+        seq_ptr = seqlens.data_ptr()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ns = int(num_splits)
+    o_part = _out(o_part, (ns, B, Hq, D), q.device, "o_part")
+    lse_part = _out(lse_part, (ns, B, Hq), q.device, "lse_part")
+    o = _out(o, (B, Hq, D), q.device, "o")
+    lse = _out(lse, (B, Hq), q.device, "lse")
+    lib = load_library()
+    n = ctypes.c_int(0)
+    _raise_if(lib.attn_decode_fused_counters(B, Hq, Hkv, ctypes.byref(n)),
+              "attn_decode_fused_counters")
+    if counters is None:
+        counters = _stream_counters(q.device, stream, n.value)
+    _check(isinstance(counters, torch.Tensor) and counters.is_cuda
+           and counters.dtype == torch.int32 and counters.is_contiguous()
+           and counters.numel() >= n.value and counters.device == q.device,
+           f"counters must be a contiguous int32 CUDA tensor with >= {n.value} entries")
+    with torch.cuda.device(q.device):
+        st = lib.attn_decode_fused(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_ptr,
+                                   o.data_ptr(), lse.data_ptr(), o_part.data_ptr(),
+                                   lse_part.data_ptr(), counters.data_ptr(), B, Hq, Hkv, Sk, D,
+                                   ns, float(scale), _stream_handle(stream))
+    _raise_if(st, "attn_decode_fused")
+    return o, lse
+
+
 def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, num_splits: int | None = None,
            scale: float | None = None, workspace=None, o=None, lse=None, stream=None,
            seqlens: torch.Tensor | None = None):
-    """Split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq]).
+    """Split-KV decode with the LSE combine fused in (one launch, attn_decode_fused);
+    returns (o [B,Hq,D], lse [B,Hq]).
 
     With ``seqlens`` (int32 CUDA [B]) sequence b attends to its first seqlens[b] keys.
-    ``num_splits=None`` picks attn_decode_num_splits for the shape.
+    ``num_splits=None`` picks attn_decode_num_splits for the shape; ``workspace`` is
+    an optional (o_part, lse_part) pair for the partials.
     """
     if num_splits is None:
         num_splits = attn_decode_num_splits(q.shape[0], q.shape[1], k.shape[1], k.shape[2],
                                             k.shape[3], q.device)
     o_part, lse_part = (None, None) if workspace is None else workspace
-    if seqlens is None:
-        o_part, lse_part = attn_decode_splitkv(q, k, v, num_splits, scale, o_part, lse_part,
-                                               stream)
-    else:
-        o_part, lse_part = attn_decode_splitkv_varlen(q, k, v, seqlens, num_splits, scale,
-                                                      o_part, lse_part, stream)
-    return attn_combine(o_part, lse_part, o, lse, stream)
+    return attn_decode_fused(q, k, v, num_splits, scale, seqlens, o_part, lse_part, o, lse,
+                             stream=stream)
 
 
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,

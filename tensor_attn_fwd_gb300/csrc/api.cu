@@ -309,6 +309,35 @@ int attn_decode_splitkv_varlen(const void* q, const void* k, const void* v, cons
                        stream);
 }
 
+int attn_decode_fused(const void* q, const void* k, const void* v, const int* seqlens, float* o,
+                      float* lse, float* o_part, float* lse_part, int* counters, int B, int Hq,
+                      int Hkv, int Sk, int D, int num_splits, float scale, void* stream) {
+  if (!o_part || !lse_part || !o || !lse || !counters) return ATTN_ERR_INVALID_ARG;
+  const int chk = decode_check_args(q, k, v, B, Hq, Hkv, Sk, D, num_splits, scale, false);
+  if (chk != ATTN_OK) return chk;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(counters) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (seqlens != nullptr && (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const FusedCombine fused{o, lse, counters};
+  const cudaError_t e =
+      launch_decode_splitkv(q, k, v, o_part, lse_part, B, Hq, Hkv, Sk, D, num_splits, scale,
+                            static_cast<cudaStream_t>(stream), status, seqlens, nullptr, &fused);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode_fused_counters(int B, int Hq, int Hkv, int* count) {
+  if (count == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(B) * Hkv * ((Hq / Hkv + 15) / 16);
+  if (n > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
+  *count = static_cast<int>(n);
+  return ATTN_OK;
+}
+
 int attn_decode_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
                               const int* block_table, const int* seqlens, float* o_part,
                               float* lse_part, int B, int Hq, int Hkv, int num_pages,

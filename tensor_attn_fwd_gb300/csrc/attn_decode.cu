@@ -99,7 +99,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                           float* __restrict__ lse_part, const int* __restrict__ seqlens,
                           const int* __restrict__ block_table, int page_size, int max_pages,
                           int num_pages, int B, int Hq, int Hkv, int Sk, int num_splits,
-                          int head_slices, float scale_log2, int* status) {
+                          int head_slices, float scale_log2, int* status,
+                          float* __restrict__ o_final, float* __restrict__ lse_final,
+                          int* __restrict__ counters) {
   using C = DecCfg<D>;
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NT = D / 8;   // n-tiles of O += P V
@@ -422,7 +424,122 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         lse_part[row] = lse;
     }
   }
-  // The combine kernel may now be scheduled; it waits for this grid to finish.
+
+  // Fused combine (counters != nullptr): the CTA that completes a (batch, KV
+  // head, head slice) group last merges the group's partials and resets the
+  // group's counter for the next call.  After the CTA barrier one thread counts
+  // the CTA in with an acquire-release atomic at GPU scope: the release
+  // publishes every thread's partial stores (ordered before it by the
+  // barrier), the acquire in the last CTA makes every other CTA's visible.
+  // The merge is combine_kernel's, warp by warp over the rows (lanes over the
+  // splits), so both paths give the same bits; it reads through L2 (ld.cg).
+  if (counters != nullptr) {
+    __shared__ int s_last;
+    __syncthreads();
+    int* counter = counters + blockIdx.z * gridDim.y + blockIdx.y;
+    if (threadIdx.x == 0) {
+      int prev;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                   : "=r"(prev) : "l"(counter) : "memory");
+      s_last = prev == num_splits - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+      // Warp w merges rows w, w + 4, w + 8, w + 12 of the slice together (their
+      // loads in flight at once), each in combine_kernel's order.
+      constexpr int DPL = D / 32;
+      constexpr int RPW = kRows / kWarps;
+      constexpr float kLog2e = 1.4426950408889634f;
+      const size_t split_rows = static_cast<size_t>(B) * Hq;  // rows per split
+      bool valid[RPW];
+      size_t row0[RPW];  // split 0's row
+      float M[RPW], W[RPW], out[RPW][DPL];
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        const int hl = slice * kRows + warp + kWarps * i;
+        valid[i] = hl < G;
+        row0[i] = static_cast<size_t>(b) * Hq + g * G + (valid[i] ? hl : 0);
+        M[i] = -INFINITY;
+        W[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) out[i][e] = 0.f;
+      }
+      for (int s = lane; s < num_splits; s += 32)
+#pragma unroll
+        for (int i = 0; i < RPW; ++i)
+          if (valid[i]) M[i] = fmaxf(M[i], __ldcg(lse_part + s * split_rows + row0[i]));
+#pragma unroll
+      for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], off));
+      for (int c0 = 0; c0 < num_splits; c0 += 32) {
+        const int s_lane = c0 + lane;
+        float w_lane[RPW];
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+          w_lane[i] = valid[i] && M[i] != -INFINITY && s_lane < num_splits
+                          ? ex2((__ldcg(lse_part + s_lane * split_rows + row0[i]) - M[i]) * kLog2e)
+                          : 0.f;
+          W[i] += w_lane[i];
+        }
+        const int cnt = min(32, num_splits - c0);
+#pragma unroll 4
+        for (int kk = 0; kk < cnt; ++kk) {
+#pragma unroll
+          for (int i = 0; i < RPW; ++i) {
+            const float w = __shfl_sync(0xffffffffu, w_lane[i], kk);
+            if (!valid[i] || M[i] == -INFINITY) continue;
+            const float* src = o_part + ((c0 + kk) * split_rows + row0[i]) * D + lane * DPL;
+            if constexpr (DPL >= 4) {
+#pragma unroll
+              for (int e = 0; e < DPL; e += 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
+                out[i][e] = fmaf(w, x.x, out[i][e]);
+                out[i][e + 1] = fmaf(w, x.y, out[i][e + 1]);
+                out[i][e + 2] = fmaf(w, x.z, out[i][e + 2]);
+                out[i][e + 3] = fmaf(w, x.w, out[i][e + 3]);
+              }
+            } else {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+              out[i][0] = fmaf(w, x.x, out[i][0]);
+              out[i][1] = fmaf(w, x.y, out[i][1]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        if (!valid[i]) continue;  // uniform in the warp
+        float L = -INFINITY;
+        if (M[i] != -INFINITY) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) W[i] += __shfl_xor_sync(0xffffffffu, W[i], off);
+          const float inv = 1.f / W[i];
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) out[i][e] *= inv;
+          L = M[i] + logf(W[i]);
+        }
+        float* dst = o_final + row0[i] * D + lane * DPL;
+        if (store_in_bounds(dst, DPL * 4, o_final, split_rows * D * sizeof(float), status)) {
+          if constexpr (DPL >= 4) {
+#pragma unroll
+            for (int e = 0; e < DPL; e += 4)
+              *reinterpret_cast<float4*>(dst + e) =
+                  make_float4(out[i][e], out[i][e + 1], out[i][e + 2], out[i][e + 3]);
+          } else {
+            *reinterpret_cast<float2*>(dst) = make_float2(out[i][0], out[i][1]);
+          }
+        }
+        if (lane == 0 && store_in_bounds(lse_final + row0[i], 4, lse_final,
+                                         split_rows * sizeof(float), status))
+          lse_final[row0[i]] = L;
+      }
+      if (threadIdx.x == 0) *counter = 0;
+    }
+  }
+  // The next kernel in the stream (the combine, when not fused) may now be
+  // scheduled; it waits for this grid to finish.
   grid_launch_dependents();
 }
 
@@ -505,7 +622,7 @@ template <int D>
 cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, const int* seqlens,
                                const PagedKV* paged, float* o_part, float* lse_part, int B,
                                int Hq, int Hkv, int Sk, int num_splits, float scale,
-                               cudaStream_t stream, int* status) {
+                               cudaStream_t stream, int* status, const FusedCombine* fused) {
   using C = DecCfg<D>;
   const int G = Hq / Hkv;
   const int head_slices = (G + kRows - 1) / kRows;
@@ -527,7 +644,8 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, cons
       static_cast<const __nv_bfloat16*>(q), o_part, lse_part, seqlens,
       paged != nullptr ? paged->block_table : nullptr, paged != nullptr ? paged->page_size : 0,
       paged != nullptr ? paged->max_pages : 0, paged != nullptr ? paged->num_pages : 0, B, Hq, Hkv,
-      Sk, num_splits, head_slices, scale_log2, status);
+      Sk, num_splits, head_slices, scale_log2, status, fused != nullptr ? fused->o : nullptr,
+      fused != nullptr ? fused->lse : nullptr, fused != nullptr ? fused->counters : nullptr);
 }
 
 }  // namespace
@@ -535,15 +653,16 @@ cudaError_t launch_decode_impl(const void* q, const void* k, const void* v, cons
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
                                   int num_splits, float scale, cudaStream_t stream, int* status,
-                                  const int* seqlens, const PagedKV* paged) {
+                                  const int* seqlens, const PagedKV* paged,
+                                  const FusedCombine* fused) {
   if (D == 256)
     return launch_decode_impl<256>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
-                                   num_splits, scale, stream, status);
+                                   num_splits, scale, stream, status, fused);
   if (D == 128)
     return launch_decode_impl<128>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
-                                   num_splits, scale, stream, status);
+                                   num_splits, scale, stream, status, fused);
   return launch_decode_impl<64>(q, k, v, seqlens, paged, o_part, lse_part, B, Hq, Hkv, Sk,
-                                num_splits, scale, stream, status);
+                                num_splits, scale, stream, status, fused);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, float* o, float* lse,

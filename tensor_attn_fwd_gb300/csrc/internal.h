@@ -124,10 +124,19 @@ int decode_check_args(const void* q, const void* k, const void* v, int B, int Hq
 
 // seqlens: optional device int32 [B] of per-sequence key counts (nullptr: Sk).
 // paged: optional page layout (then Sk = max_pages * page_size, the capacity).
+// fused: when counters != nullptr, the CTA that completes a (batch, KV head,
+// 16-head slice) group last also combines the group's partials into o / lse
+// (counters: int32 [B * Hkv * ceil((Hq/Hkv)/16)], zero on entry, zero again after).
+struct FusedCombine {
+  float* o;
+  float* lse;
+  int* counters;
+};
 cudaError_t launch_decode_splitkv(const void* q, const void* k, const void* v, float* o_part,
                                   float* lse_part, int B, int Hq, int Hkv, int Sk, int D,
                                   int num_splits, float scale, cudaStream_t stream, int* status,
-                                  const int* seqlens = nullptr, const PagedKV* paged = nullptr);
+                                  const int* seqlens = nullptr, const PagedKV* paged = nullptr,
+                                  const FusedCombine* fused = nullptr);
 
 // Backward: Delta into `delta` ([B,Hq,Sq]), then dK/dV and dQ kernels.
 cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const float* o,

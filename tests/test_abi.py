@@ -142,6 +142,56 @@ def test_decode_noalloc_matches_decode_checks(lib):
         assert noalloc(lib, **kw) == dec(lib, **kw)
 
 
+def fused(lib, q=A, k=A, v=A, sl=None, o=A, lse=A, op=A, lp=A, cnt=A, B=1, Hq=4, Hkv=1, Sk=64,
+          D=128, ns=4, scale=0.1):
+    return lib.attn_decode_fused(q, k, v, sl, o, lse, op, lp, cnt, B, Hq, Hkv, Sk, D, ns, scale,
+                                 None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cnt=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(op=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ns=65), attn.ATTN_ERR_INVALID_ARG),   # more splits than keys
+    (dict(Hq=6, Hkv=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(B=70000), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Sk=(1 << 30) + 1, ns=8), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(k=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(o=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(lse=M), attn.ATTN_ERR_MISALIGNED),
+    (dict(cnt=A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(sl=A + 2), attn.ATTN_ERR_MISALIGNED),
+])
+def test_decode_fused_rejects(lib, kw, code):
+    assert fused(lib, **kw) == code
+
+
+def test_decode_fused_matches_decode_checks(lib):
+    # The fused decode rejects every input the two-launch decode rejects, with
+    # the same status.
+    for kw in (dict(Sk=(1 << 30) + 1, ns=8), dict(D=96), dict(Hq=6, Hkv=4), dict(ns=0),
+               dict(q=M), dict(scale=0.0), dict(B=70000)):
+        assert fused(lib, **kw) == dec(lib, **kw)
+
+
+def test_decode_fused_counters(lib):
+    n = ctypes.c_int(0)
+    assert lib.attn_decode_fused_counters(64, 32, 8, ctypes.byref(n)) == attn.ATTN_OK
+    assert n.value == 64 * 8          # group of 4 query heads: one 16-head slice
+    assert lib.attn_decode_fused_counters(2, 64, 2, ctypes.byref(n)) == attn.ATTN_OK
+    assert n.value == 2 * 2 * 2       # group of 32: two slices
+    assert lib.attn_decode_fused_counters(1, 17, 1, ctypes.byref(n)) == attn.ATTN_OK
+    assert n.value == 2
+    assert lib.attn_decode_fused_counters(1, 6, 4, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_fused_counters(0, 4, 1, ctypes.byref(n)) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_decode_fused_counters(1, 4, 1, None) == attn.ATTN_ERR_INVALID_ARG
+
+
 def comb(lib, op=A, lp=A, o=A, lse=A, B=1, Hq=4, D=128, ns=4):
     return lib.attn_combine(op, lp, o, lse, B, Hq, D, ns, None)
 
