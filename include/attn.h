@@ -295,6 +295,19 @@ ATTN_API int attn_decode_fused(const void *q, const void *k, const void *v, cons
                                int num_splits, float scale, void *stream);
 
 /*
+ * attn_decode_fused over a paged cache: the partials of
+ * attn_decode_splitkv_paged (its cache layout, block table, sequence lengths
+ * and split rule) and their combine in one launch, with o, lse and counters
+ * as attn_decode_fused.  Returns the argument errors of both.
+ */
+ATTN_API int attn_decode_fused_paged(const void *q, const void *k_cache, const void *v_cache,
+                                     const int *block_table, const int *seqlens, float *o,
+                                     float *lse, float *o_part, float *lse_part, int *counters,
+                                     int B, int Hq, int Hkv, int num_pages, int page_size,
+                                     int max_pages, int D, int num_splits, float scale,
+                                     void *stream);
+
+/*
  * Number of int32 counters attn_decode_fused needs: B * Hkv * ceil((Hq/Hkv)/16).
  * Host-only.  ATTN_ERR_INVALID_ARG for non-positive sizes or Hq % Hkv != 0.
  */

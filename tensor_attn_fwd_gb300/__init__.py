@@ -68,6 +68,7 @@ _SIGNATURES = {
     "attn_combine": ([_vp, _vp, _vp, _vp, _int, _int, _int, _int, _vp], _int),
     "attn_decode_fused": ([_vp] * 9 + [_int] * 6 + [_flt, _vp], _int),
     "attn_decode_fused_counters": ([_int, _int, _int, ctypes.POINTER(_int)], _int),
+    "attn_decode_fused_paged": ([_vp] * 10 + [_int] * 8 + [_flt, _vp], _int),
     "attn_fwd_splitkv": ([_vp] * 5 + [_int] * 8 + [_flt, _vp], _int),
     "attn_fwd_num_splits": ([_int] * 6 + [ctypes.POINTER(_int)], _int),
     "attn_rope_table": ([_vp, _int, _int, _flt, _vp], _int),
@@ -395,12 +396,56 @@ def attn_decode_splitkv_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
 
 def decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  block_table: torch.Tensor, seqlens: torch.Tensor, num_splits: int,
-                 scale: float | None = None, workspace=None, o=None, lse=None, stream=None):
-    """Paged split-KV decode followed by the LSE combine; returns (o [B,Hq,D], lse [B,Hq])."""
+                 scale: float | None = None, workspace=None, o=None, lse=None, stream=None,
+                 counters: torch.Tensor | None = None):
+    """Paged split-KV decode with the LSE combine fused in (one launch,
+    attn_decode_fused_paged); returns (o [B,Hq,D], lse [B,Hq]).
+
+    Cache layout and arguments as attn_decode_splitkv_paged; ``workspace`` is an
+    optional (o_part, lse_part) pair for the partials, ``counters`` as
+    attn_decode_fused.
+    """
+    _check_bf16("q", q, 4)
+    _check_bf16("k_cache", k_cache, 4)
+    _check_bf16("v_cache", v_cache, 4)
+    B, Hq, Sq, D = q.shape
+    _check(Sq == 1, "decode takes one query row per head (q.shape[2] == 1)")
+    num_pages, Hkv, page_size, Dk = k_cache.shape
+    _check(Dk == D and tuple(v_cache.shape) == tuple(k_cache.shape), "q/cache shape mismatch")
+    for name, t in (("block_table", block_table), ("seqlens", seqlens)):
+        _check(isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32
+               and t.is_contiguous() and t.device == q.device,
+               f"{name} must be a contiguous int32 tensor on q's device")
+    _check(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_pages]")
+    _check(tuple(seqlens.shape) == (B,), "seqlens must be [B]")
+    _check(k_cache.device == q.device and v_cache.device == q.device, "q and caches must share a device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ns = int(num_splits)
     o_part, lse_part = (None, None) if workspace is None else workspace
-    o_part, lse_part = attn_decode_splitkv_paged(q, k_cache, v_cache, block_table, seqlens,
-                                                 num_splits, scale, o_part, lse_part, stream)
-    return attn_combine(o_part, lse_part, o, lse, stream)
+    o_part = _out(o_part, (ns, B, Hq, D), q.device, "o_part")
+    lse_part = _out(lse_part, (ns, B, Hq), q.device, "lse_part")
+    o = _out(o, (B, Hq, D), q.device, "o")
+    lse = _out(lse, (B, Hq), q.device, "lse")
+    lib = load_library()
+    n = ctypes.c_int(0)
+    _raise_if(lib.attn_decode_fused_counters(B, Hq, Hkv, ctypes.byref(n)),
+              "attn_decode_fused_counters")
+    if counters is None:
+        counters = _stream_counters(q.device, stream, n.value)
+    _check(isinstance(counters, torch.Tensor) and counters.is_cuda
+           and counters.dtype == torch.int32 and counters.is_contiguous()
+           and counters.numel() >= n.value and counters.device == q.device,
+           f"counters must be a contiguous int32 CUDA tensor with >= {n.value} entries")
+    with torch.cuda.device(q.device):
+        st = lib.attn_decode_fused_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         block_table.data_ptr(), seqlens.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), o_part.data_ptr(), lse_part.data_ptr(),
+                                         counters.data_ptr(), B, Hq, Hkv, num_pages, page_size,
+                                         block_table.shape[1], D, ns, float(scale),
+                                         _stream_handle(stream))
+    _raise_if(st, "attn_decode_fused_paged")
+    return o, lse
 
 
 def attn_rope_table(max_pos: int, D: int, base: float = 10000.0, device=None,

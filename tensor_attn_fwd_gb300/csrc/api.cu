@@ -338,29 +338,76 @@ int attn_decode_fused_counters(int B, int Hq, int Hkv, int* count) {
   return ATTN_OK;
 }
 
-int attn_decode_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
-                              const int* block_table, const int* seqlens, float* o_part,
-                              float* lse_part, int B, int Hq, int Hkv, int num_pages,
-                              int page_size, int max_pages, int D, int num_splits, float scale,
-                              void* stream) {
+namespace {
+
+// The paged decode entry points' checks of the cache description; ATTN_OK or
+// the status to return.  On success *paged describes the cache and *capacity is
+// max_pages * page_size.
+int paged_check_args(const int* block_table, const int* seqlens, int Hkv, int num_pages,
+                     int page_size, int max_pages, int D, int B, PagedKV* paged, int* capacity) {
   if (!block_table || !seqlens) return ATTN_ERR_INVALID_ARG;
   if (num_pages <= 0 || page_size <= 0 || max_pages <= 0) return ATTN_ERR_INVALID_ARG;
   if (page_size % 32 != 0) return ATTN_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
       (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0)
     return ATTN_ERR_MISALIGNED;
-  const long long capacity = static_cast<long long>(max_pages) * page_size;
-  if (capacity > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+  const long long cap = static_cast<long long>(max_pages) * page_size;
+  if (cap > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
   if (Hkv > 0 && static_cast<long long>(num_pages) * Hkv > (1ll << 30)) return ATTN_ERR_UNSUPPORTED;
   if (Hkv > 0 && D > 0 &&
       static_cast<long long>(num_pages) * Hkv * page_size * D > kMaxElems)
     return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * max_pages > (1ll << 31) - 1) return ATTN_ERR_UNSUPPORTED;
-  const PagedKV paged{block_table, page_size, max_pages, num_pages};
+  *paged = PagedKV{block_table, page_size, max_pages, num_pages};
+  *capacity = static_cast<int>(cap);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+int attn_decode_fused_paged(const void* q, const void* k_cache, const void* v_cache,
+                            const int* block_table, const int* seqlens, float* o, float* lse,
+                            float* o_part, float* lse_part, int* counters, int B, int Hq, int Hkv,
+                            int num_pages, int page_size, int max_pages, int D, int num_splits,
+                            float scale, void* stream) {
+  PagedKV paged;
+  int capacity = 0;
+  const int pchk = paged_check_args(block_table, seqlens, Hkv, num_pages, page_size, max_pages,
+                                    D, B, &paged, &capacity);
+  if (pchk != ATTN_OK) return pchk;
+  if (!o_part || !lse_part || !o || !lse || !counters) return ATTN_ERR_INVALID_ARG;
+  // The contiguous-size checks apply to the capacity; the cache itself is
+  // num_pages pages, checked above.
+  const int chk = decode_check_args(q, k_cache, v_cache, B, Hq, Hkv, capacity, D, num_splits,
+                                    scale, true);
+  if (chk != ATTN_OK) return chk;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(counters) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  int* status = status_word_device_ptr();
+  if (status == nullptr) return ATTN_ERR_CUDA;
+  const FusedCombine fused{o, lse, counters};
+  const cudaError_t e = launch_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, B, Hq, Hkv,
+                                              capacity, D, num_splits, scale,
+                                              static_cast<cudaStream_t>(stream), status, seqlens,
+                                              &paged, &fused);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_decode_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
+                              const int* block_table, const int* seqlens, float* o_part,
+                              float* lse_part, int B, int Hq, int Hkv, int num_pages,
+                              int page_size, int max_pages, int D, int num_splits, float scale,
+                              void* stream) {
+  PagedKV paged;
+  int capacity = 0;
+  const int pchk = paged_check_args(block_table, seqlens, Hkv, num_pages, page_size, max_pages,
+                                    D, B, &paged, &capacity);
+  if (pchk != ATTN_OK) return pchk;
   // The contiguous-size checks of decode_common apply to the capacity; the
   // cache itself is num_pages pages, checked above.
-  return decode_common(q, k_cache, v_cache, seqlens, o_part, lse_part, B, Hq, Hkv,
-                       static_cast<int>(capacity), D, num_splits, scale, stream, &paged);
+  return decode_common(q, k_cache, v_cache, seqlens, o_part, lse_part, B, Hq, Hkv, capacity, D,
+                       num_splits, scale, stream, &paged);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,

@@ -179,6 +179,25 @@ def test_decode_fused_matches_decode_checks(lib):
         assert fused(lib, **kw) == dec(lib, **kw)
 
 
+def fusedp(lib, q=A, k=A, v=A, bt=A, sl=A, o=A, lse=A, op=A, lp=A, cnt=A, B=1, Hq=4, Hkv=1,
+           num_pages=8, page=64, max_pages=4, D=128, ns=4, scale=0.1):
+    return lib.attn_decode_fused_paged(q, k, v, bt, sl, o, lse, op, lp, cnt, B, Hq, Hkv, num_pages,
+                                       page, max_pages, D, ns, scale, None)
+
+
+def test_decode_fused_paged_matches_paged_checks(lib):
+    # Every cache description or argument the two-launch paged decode rejects,
+    # the fused one rejects with the same status.
+    for kw in (dict(bt=None), dict(sl=None), dict(num_pages=0), dict(page=48), dict(bt=A + 2),
+               dict(max_pages=1 << 25, page=64), dict(D=96), dict(Hq=6, Hkv=4), dict(ns=0),
+               dict(q=M), dict(scale=0.0), dict(op=M)):
+        assert fusedp(lib, **kw) == decp(lib, **kw), kw
+    assert fusedp(lib, cnt=None) == attn.ATTN_ERR_INVALID_ARG
+    assert fusedp(lib, o=None) == attn.ATTN_ERR_INVALID_ARG
+    assert fusedp(lib, lse=M) == attn.ATTN_ERR_MISALIGNED
+    assert fusedp(lib, cnt=A + 2) == attn.ATTN_ERR_MISALIGNED
+
+
 def test_decode_fused_counters(lib):
     n = ctypes.c_int(0)
     assert lib.attn_decode_fused_counters(64, 32, 8, ctypes.byref(n)) == attn.ATTN_OK

@@ -14,6 +14,7 @@ import torch
 import oracle
 import tensor_attn_fwd_gb300 as attn
 from attn_inputs import make_qkv
+from test_paged import build_paged
 from test_parity import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -134,3 +135,25 @@ def test_fused_graph_replay():
         assert attn.attn_debug_status() == attn.ATTN_OK
         assert int(counters.abs().sum()) == 0
         check_against_oracle(q, k, v, o, lse, scale, what=f"replay {rep}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,cap,D,page,ns", [
+    (6, 32, 8, 1024, 128, 64, 8),
+    (5, 4, 4, 300, 64, 32, 3),
+    (3, 16, 2, 700, 256, 128, 5),
+])
+def test_fused_paged_equals_two_launches(B, Hq, Hkv, cap, D, page, ns):
+    scale = 1.0 / math.sqrt(D)
+    q, k, v = make_qkv(B, Hq, Hkv, 1, cap, D, seed=B + cap + page)
+    lens_t = torch.tensor([cap] + [int(x) for x in torch.randint(
+        0, cap + 1, (B - 1,), generator=torch.Generator().manual_seed(cap))], dtype=torch.int32)
+    kc, vc, table = build_paged(k, v, lens_t, page, spare_pages=2, seed=cap + 1)
+    qd, kcd, vcd, td, ld = q.cuda(), kc.cuda(), vc.cuda(), table.cuda(), lens_t.cuda()
+    o, lse = attn.decode_paged(qd, kcd, vcd, td, ld, ns, scale)
+    op, lp = attn.attn_decode_splitkv_paged(qd, kcd, vcd, td, ld, ns, scale)
+    o2, lse2 = attn.attn_combine(op, lp)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    check_against_oracle(q, k, v, o, lse, scale, lens=[int(x) for x in lens_t],
+                         what=f"paged B{B} page{page} ns{ns}")
