@@ -53,7 +53,8 @@ def test_d256_bf16_output():
     torch.cuda.synchronize()
     assert attn.attn_debug_status() == attn.ATTN_OK
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, scale)
-    assert_close(o16.float().cpu().numpy(), lse16.cpu().numpy(), o_ref, lse_ref, "bf16 O")
+    assert_close(o16.float().cpu().numpy(), lse16.cpu().numpy(), o_ref, lse_ref, "bf16 O",
+                 o_bf16=True)
     assert torch.equal(o16, o32.to(torch.bfloat16))
     assert torch.equal(lse16, lse32)
 

@@ -4,6 +4,9 @@ Tolerances (bf16 inputs, fp32 accumulation, P rounded to bf16 before P*V):
   O:   max |O_gpu - O_ref| <= 2e-2
   LSE: |LSE_gpu - LSE_ref| <= 1e-3 * max(1, |LSE_ref|)
 Rows with no visible key must match exactly (O = 0, LSE = -inf).
+A bf16 O is the fp32 O rounded to nearest even (checked bit for bit), so it may
+also differ by that rounding, at most 2^-8 of its magnitude: per element
+|O_gpu - O_ref| <= 2e-2 + 2^-8 * (|O_ref| + 2e-2).
 """
 import dataclasses
 import math
@@ -20,9 +23,12 @@ pytestmark = pytest.mark.gpu
 
 O_TOL = 2e-2
 LSE_TOL = 1e-3
+BF16_REL = 2.0 ** -8  # round to nearest even into bf16's 8-bit significand
 
 
-def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", o_bf16=False):
+    """O within O_TOL (plus the bf16 rounding of the output when o_bf16), LSE
+    within LSE_TOL relative to max(1, |LSE_ref|), the -inf pattern exact."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
     assert o_gpu.shape == o_ref.shape and lse_gpu.shape == lse_ref.shape
@@ -31,7 +37,13 @@ def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert np.array_equal(np.isfinite(lse_gpu), fin), f"{what}: -inf pattern differs"
     assert np.all(lse_gpu[~fin] == -np.inf)
     err_o = float(np.max(np.abs(o_gpu - o_ref))) if o_gpu.size else 0.0
-    assert err_o <= O_TOL, f"{what}: O max-abs error {err_o:.3e} > {O_TOL}"
+    if o_bf16:
+        excess = np.abs(o_gpu - o_ref) - (O_TOL + BF16_REL * (np.abs(o_ref) + O_TOL))
+        worst = float(np.max(excess)) if o_gpu.size else -1.0
+        assert worst <= 0.0, (f"{what}: bf16 O error {err_o:.3e} beyond 2e-2 plus the output "
+                              f"rounding (by {worst:.3e})")
+    else:
+        assert err_o <= O_TOL, f"{what}: O max-abs error {err_o:.3e} > {O_TOL}"
     if np.any(fin):
         d = np.abs(lse_gpu[fin] - lse_ref[fin]) / np.maximum(1.0, np.abs(lse_ref[fin]))
         assert float(d.max()) <= LSE_TOL, f"{what}: LSE error {float(d.max()):.3e} > {LSE_TOL}"
@@ -281,7 +293,8 @@ def test_bf16_output(B, Hq, Hkv, Sq, Sk, D, causal):
     assert attn.attn_debug_status() == attn.ATTN_OK
     assert o16.dtype == torch.bfloat16
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
-    assert_close(o16.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16 O")
+    assert_close(o16.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16 O",
+                 o_bf16=True)
     # exactly the fp32 result rounded to nearest even
     assert torch.equal(o16, o32.to(torch.bfloat16))
     assert torch.equal(lse, lse32)

@@ -53,7 +53,9 @@ def test_prefill_chain_reads_previous_output(D, causal):
         o_ref, lse_ref = oracle.attn_fwd(x, k, v, causal, scale)
         o_gpu = ref[i][0].float().cpu().double().numpy()
         err = float(np.max(np.abs(o_gpu - o_ref)))
-        assert err <= 2e-2, f"step {i}: O max-abs error {err:.3e} against the oracle chain"
+        # 2e-2, plus the rounding of the bf16 output (2^-8 of its magnitude)
+        excess = float(np.max(np.abs(o_gpu - o_ref) - (2e-2 + 2.0 ** -8 * (np.abs(o_ref) + 2e-2))))
+        assert excess <= 0.0, f"step {i}: O max-abs error {err:.3e} against the oracle chain"
         dl = np.abs(ref[i][1].cpu().double().numpy() - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
         assert float(dl.max()) <= 1e-3, f"step {i}: LSE error {float(dl.max()):.3e}"
         x = ref[i][0].cpu()  # continue from the GPU's own bf16 O (same bits on both sides)
