@@ -4,8 +4,9 @@ paged) and the backward, each case drawn from a fixed seed so that a failure
 reproduces.  The shapes cover what the fixed cases do not reach together:
 odd lengths on both axes, Sq > Sk under the causal mask (rows that see no
 key), GQA/MQA groupings of 1-8, D = 64/128/256, scales other than 1/sqrt(D)
-and peakier inputs (std up to 2).  Tolerances are the parity tolerances (for a
-bf16 O, plus its rounding to bf16)."""
+and peakier inputs (std up to 2); and, on sampled rows, shapes large enough for
+the launch-wide work-item orders and head pairing.  Tolerances are the parity
+tolerances (for a bf16 O, plus its rounding to bf16)."""
 import math
 
 import numpy as np
@@ -14,7 +15,7 @@ import torch
 
 import oracle
 import tensor_attn_fwd_gb300 as attn
-from attn_inputs import make_qkv
+from attn_inputs import make_qkv, sample_rows
 from test_parity import assert_close
 from test_paged import build_paged
 
@@ -57,6 +58,37 @@ def test_fwd_random(i):
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, c["causal"], c["scale"])
     assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, str(c),
                  o_bf16=c["out"] == "bf16")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal,out,splits", [
+    (4, 32, 8, 4096, 4096, 256, True, "fp32", 1),     # D = 256, chunked KV-head order
+    (2, 16, 16, 4096, 4096, 256, False, "fp32", 1),   # D = 256, KV-head order
+    (8, 16, 16, 2048, 2048, 128, False, "fp32", 1),   # D = 128, KV-head order
+    (8, 16, 16, 2048, 2048, 64, False, "bf16", 1),    # D = 64, KV-head order, bf16 O
+    (2, 32, 8, 100, 8192, 128, True, "fp32", 1),      # head pairs: a chunk against a cache
+    (2, 32, 8, 100, 8192, 128, True, "fp32", 8),      # head pairs with split-KV
+    (1, 64, 8, 128, 16384, 64, True, "fp32", "auto"),
+    (3, 24, 8, 3000, 5000, 128, True, "fp32", 1),     # Sq != Sk, groups of 3
+    (2, 8, 1, 6000, 6000, 256, True, "bf16", 1),      # MQA at D = 256
+])
+def test_fwd_large_sampled(B, Hq, Hkv, Sq, Sk, D, causal, out, splits):
+    # Sizes at which the launch-wide work-item orders and head pairing take
+    # effect; 400 random rows plus every head's edge rows against the oracle.
+    seed = B * 7 + Sq + Sk + D
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Sk, D, seed)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    if out == "bf16":
+        o, lse = attn.attn_fwd_bf16o(qd, kd, vd, causal=causal, scale=scale)
+    else:
+        o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert attn.attn_debug_status() == attn.ATTN_OK
+    rows = sample_rows(B, Hq, Sq, 400, seed)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale, rows=rows.numpy())
+    assert_close(o.float().reshape(-1, D)[rows].cpu().numpy(), lse.reshape(-1)[rows].cpu().numpy(),
+                 o_ref, lse_ref, f"B{B} Hq{Hq} Hkv{Hkv} Sq{Sq} Sk{Sk} D{D} c{causal} {out}",
+                 o_bf16=out == "bf16")
 
 
 @pytest.mark.parametrize("i", range(48))
