@@ -538,6 +538,31 @@ def ours_arm(args, rank, world, local_rank, dist_on):
                     ev_out[i].record(s_out)
             return ev_out[-1]
 
+        # The host link's own rates on this machine, for reading the e2e number: one
+        # timed copy of the step's inputs in and of its outputs back, each alone.
+        def link_gbs(copy, nbytes):
+            copy()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s_in)
+            copy()
+            b.record(s_in)
+            torch.cuda.synchronize()
+            return nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+
+        def copy_in():
+            with torch.cuda.stream(s_in):
+                sets[0][0].copy_(qp, non_blocking=True)
+                sets[0][1].copy_(kp, non_blocking=True)
+                sets[0][2].copy_(vp, non_blocking=True)
+
+        def copy_out():
+            with torch.cuda.stream(s_in):
+                op_h.copy_(sets[0][3], non_blocking=True)
+                lp_h.copy_(sets[0][4], non_blocking=True)
+
+        link = {"h2d_gbs": link_gbs(copy_in, sum(t.numel() * t.element_size() for t in (qp, kp, vp))),
+                "d2h_gbs": link_gbs(copy_out, op_h.numel() * 4 + lp_h.numel() * 4)}
         e_steps = max(4, min(args.steps, 20))
         e2e_run(3)  # warm-up
         torch.cuda.synchronize()
@@ -556,10 +581,10 @@ def ours_arm(args, rank, world, local_rank, dist_on):
         d2h = op_h.numel() * 4 + lp_h.numel() * 4
         e2e = {"value": flops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e_ms, "steps": e_steps, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h,
+               "d2h_bytes_per_step": d2h, "host_link": link,
                "method": "pinned host buffers; H2D, attn_fwd and D2H on three streams, "
                          "two device buffer sets, timed from the first copy in to the "
-                         "last copy out"}
+                         "last copy out; host_link: one copy in and one out, each alone"}
         del sets
     # ---------------- the other workloads (1, 2, 4): GPU time and output
     cfg_runs = {}
