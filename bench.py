@@ -58,7 +58,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # `bench.py --profile prefill|decode`; profiles/ holds the summary.  Reset to
 # None whenever the kernel changes until it is captured again.
 PREFILL_TRAFFIC_BYTES = 319545344 + 214419968
-DECODE_TRAFFIC_BYTES = 1074305024 + 10365184
+DECODE_TRAFFIC_BYTES = 1074342656 + 11164928
 
 
 def load_peaks():
