@@ -536,22 +536,28 @@ def attn_decode_num_splits(B: int, Hq: int, Hkv: int, Sk: int, D: int = 128,
 
 # Zeroed int32 counter arrays for attn_decode_fused, one per (device, stream):
 # a call leaves its counters zero, so calls on one stream share an array and
-# calls on different streams (which may overlap) never do.
+# calls on different streams (which may overlap) never do.  At most
+# _COUNTERS_KEPT streams are remembered (the least recently used is dropped;
+# its array was allocated on its own stream, so the allocator reuses it only
+# after that stream's work).
 _counters = {}
 _counters_lock = threading.Lock()
+_COUNTERS_KEPT = 256
 
 
 def _stream_counters(device: torch.device, stream, n: int) -> torch.Tensor:
     handle = _stream_handle(stream)
     key = (device.index, handle)
     with _counters_lock:
-        buf = _counters.get(key)
+        buf = _counters.pop(key, None)
         if buf is None or buf.numel() < n:
             # Zeroed on the call's own stream, so the memset precedes the kernel.
             with torch.cuda.device(device), torch.cuda.stream(
                     torch.cuda.ExternalStream(handle, device=device)):
                 buf = torch.zeros(max(n, 1024), dtype=torch.int32, device=device)
-            _counters[key] = buf
+        _counters[key] = buf  # most recently used last
+        while len(_counters) > _COUNTERS_KEPT:
+            _counters.pop(next(iter(_counters)))
     return buf
 
 
