@@ -267,8 +267,11 @@ ATTN_API int attn_combine(const float *o_part, const float *lse_part, float *o, 
 /*
  * Decode in one launch: the split-KV partials of attn_decode_splitkv (or, with
  * seqlens, of attn_decode_splitkv_varlen), and their log-sum-exp combine
- * (attn_combine's formula).  Source: the same pages (FlashDecoding: per-split
- * partials, then the reduction across splits).  The combine of each (batch, KV
+ * (attn_combine's formula).  Source: "A Thread-Register Decoupled GPU
+ * Execution Model for Efficient Tensor Computation", Methodology and
+ * Evaluation (FlashDecoding: per-split partials, then the reduction across
+ * splits); with seqlens, "VDCores: Resource Decoupled Programming and
+ * Execution for Asynchronous GPUs", Evaluation (dynamic attention length).  The combine of each (batch, KV
  * head, 16-query-head slice) group runs in the CTA that completes the group's
  * last split, found with one int32 counter per group, so it overlaps the
  * streaming of other groups and needs no second kernel.
@@ -298,7 +301,9 @@ ATTN_API int attn_decode_fused(const void *q, const void *k, const void *v, cons
  * attn_decode_fused over a paged cache: the partials of
  * attn_decode_splitkv_paged (its cache layout, block table, sequence lengths
  * and split rule) and their combine in one launch, with o, lse and counters
- * as attn_decode_fused.  Returns the argument errors of both.
+ * as attn_decode_fused.  Source: as attn_decode_splitkv_paged ("VDCores:
+ * Resource Decoupled Programming and Execution for Asynchronous GPUs",
+ * Evaluation) and attn_combine.  Returns the argument errors of both.
  */
 ATTN_API int attn_decode_fused_paged(const void *q, const void *k_cache, const void *v_cache,
                                      const int *block_table, const int *seqlens, float *o,
